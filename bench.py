@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the paged KV-cache attention library.
+
+One step = the whole hot path over one batch: the cache write of every
+sequence's new token (reshape_and_cache) followed by paged decode attention
+(plus its log-sum-exp combine when the context is partitioned).  Inputs are
+seeded synthetic workloads resident in HBM before timing starts.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle as the reference arm
+
+For N > 1 launch under torchrun; every rank runs its own batch (weak
+scaling, no collective on the data path) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+DEFAULT_WORKLOAD = "mha_7b"
+METRIC = "paged decode attention effective KV-read GB/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per decode launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by workload, valid only while the kernel
+# sources hash to `src`.  Filled in from the profiles summaries.
+NCU_TRAFFIC: dict = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_249_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_gbs() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed
+    region runs (read-only queries; no setting is changed)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int = 0, period_ms: int = 20):
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.window = (0.0, 0.0)
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={uuid}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 5.0:
+                time.sleep(0.02)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def mark_start(self):
+        self.window = (time.monotonic(), self.window[1])
+
+    def mark_end(self):
+        self.window = (self.window[0], time.monotonic())
+        time.sleep(0.05)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        t0, t1 = self.window
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = "timed region"
+        if not inside and self.samples:  # timed region shorter than the sampling period
+            nearest = min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))
+            inside = [nearest[1]]
+            note = "nearest sample (timed region shorter than the sampling period)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[1]) for s in inside if len(s) > 8 and num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if len(s) > 8 and num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside if len(s) > 8
+                          for i, v in enumerate(s[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": note}
+
+
+# ----------------------------------------------------------------- ranks --
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (the job is as slow as its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------ workloads --
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes the decode step must move at minimum (per rank, per step)."""
+    e = w.elem_bytes
+    kv_logical = w.kv_bytes_logical()
+    kv_unique = w.kv_bytes_unique()
+    q = w.num_seqs * w.num_heads * w.head_dim * e
+    out = w.num_seqs * w.num_heads * w.head_dim * 2  # bf16 output
+    table = int(np.sum((w.context_lens.astype(np.int64) + w.block_size - 1) // w.block_size)) * 4
+    new_kv = 2 * w.num_seqs * w.num_kv_heads * w.head_dim * e
+    return {"kv_logical": kv_logical, "kv_unique": kv_unique, "q": q, "out": out,
+            "table": table, "new_kv": new_kv,
+            "decode_launch": kv_unique + q + out + table + w.num_seqs * 4}
+
+
+def workload_config(w, name: str, world: int) -> dict:
+    from paged_kv_cache_249_gb300 import workload as wl
+    return {"workload": f"{name}: {wl.WORKLOADS[name]['desc']}", "num_seqs": w.num_seqs,
+            "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "kv_dtype": w.dtype, "out_dtype": "bf16",
+            "accumulate": "f32", "mean_context": float(w.context_lens.mean()),
+            "kv_bytes_per_step": w.kv_bytes_logical(),
+            "partition_tokens": w.partition_tokens or "auto",
+            "l2": f"inputs larger than L2 ({w.kv_bytes_unique() / 1e6:.0f} MB of unique KV per "
+                  "step vs 129 MB L2); no flush",
+            "parallelism": f"replicas x{world} (each rank its own batch)"}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def _oracle_sample(w, target_s: float, threads: int):
+    """Pick a prefix of the batch whose oracle run takes about target_s."""
+    import oracle
+    from paged_kv_cache_249_gb300 import workload as wl
+    first = wl.subset(w, [0])
+    t0 = time.perf_counter()
+    oracle.paged_decode(first.q, w.k_pool, w.v_pool, first.block_tables, first.context_lens,
+                        w.scale, num_threads=threads)
+    per_token = (time.perf_counter() - t0) / max(1, int(w.context_lens[0]))
+    budget_tokens = target_s / max(per_token, 1e-12)
+    csum = np.cumsum(w.context_lens.astype(np.int64))
+    n = int(np.searchsorted(csum, budget_tokens, side="right"))
+    n = max(1, min(w.num_seqs, n))
+    return wl.subset(w, range(n)), n
+
+
+def _oracle_time(sub, w, threads: int) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.paged_decode(sub.q, w.k_pool, w.v_pool, sub.block_tables, sub.context_lens, w.scale,
+                        num_threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, target_s: float = 12.0) -> dict:
+    """The float64 oracle as it stands, timed on this host's cores on a
+    bounded prefix of the same batch."""
+    threads = os.cpu_count() or 1
+    sub, n = _oracle_sample(w, target_s, threads)
+    secs = _oracle_time(sub, w, threads)
+    kv = sub.kv_bytes_logical()
+    return {"value": kv / secs / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {w.num_seqs} sequences ({kv / 1e9:.3f} GB of KV), "
+                      f"{secs:.2f} s on {threads} threads", "seqs_per_s": n / secs}
+
+
+# ---------------------------------------------------------------- native --
+
+def run_native(args, world: int, rank: int) -> dict | None:
+    from paged_kv_cache_249_gb300 import build as pkv_build
+    from paged_kv_cache_249_gb300 import pagedkv
+    from paged_kv_cache_249_gb300 import workload as wl
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the native arm needs a CUDA device")
+    pkv_build.build()
+    pagedkv.load()
+    w = wl.make(args.workload)
+    # the cache write must land where the oracle-side copy can still see
+    # the untouched pools for the CPU baseline
+    dw = pagedkv.DeviceWorkload(w, out_dtype=torch.bfloat16)
+    split = dw.workspace is not None
+    launches_per_step = 2 + (1 if split else 0)
+    stream = torch.cuda.current_stream()
+    ab = algorithmic_bytes(w)
+
+    for _ in range(args.warmup):
+        dw.step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
+    t_start.record(stream)
+    for k in range(args.steps):
+        pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+        ev_dec[k][0].record(stream)
+        dw.decode()
+        ev_dec[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    clock_info = clocks.stop() if clocks else None
+    fault = pagedkv.get_device_error(dw.pool)
+    if fault:
+        raise SystemExit(f"bench.py: device fault bits {fault}")
+
+    max_s = max_over_ranks(total_ms / 1e3, world)
+    ms_per_step = max_s * 1e3 / args.steps
+    value = whole_job_rate(ab["kv_logical"] * args.steps, world, max_s) / 1e9
+    seqs_per_s = whole_job_rate(w.num_seqs * args.steps, world, max_s)
+
+    # ---- end to end through the C ABI with host buffers
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    q_h, nk_h, nv_h = pin(w.q), pin(w.new_key), pin(w.new_value)
+    sm_h = pin(torch.from_numpy(w.slot_mapping))
+    cl_h = pin(torch.from_numpy(w.context_lens))
+    bt_h = pin(torch.from_numpy(w.block_tables))
+    out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, nk_h, nv_h, sm_h, cl_h, bt_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        dw.q.copy_(q_h, non_blocking=True)
+        dw.new_key.copy_(nk_h, non_blocking=True)
+        dw.new_value.copy_(nv_h, non_blocking=True)
+        dw.slot_mapping.copy_(sm_h, non_blocking=True)
+        dw.context_lens.copy_(cl_h, non_blocking=True)
+        pagedkv.block_table_upload(dw.block_tables, bt_h, w.num_blocks)
+        dw.step()
+        out_h.copy_(dw.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = whole_job_rate(ab["kv_logical"] * args.steps, world, e2e_s) / 1e9
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak_gbs()
+    dec_avg_s = float(np.mean(dec_ms)) / 1e3
+    achieved = ab["decode_launch"] / dec_avg_s / 1e9
+    traffic = None
+    rec = NCU_TRAFFIC.get(args.workload)
+    if rec and rec.get("src") == kernel_source_hash():
+        traffic = rec["bytes"]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), PCG64)",
+        "config": workload_config(w, args.workload, world),
+        "seqs_per_s": round(seqs_per_s, 1),
+        "pct_hbm_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6800 GB/s",
+                     "kernel": "paged_decode_kernel (+ lse_combine when split)",
+                     "algorithmic_bytes_per_launch": ab["decode_launch"],
+                     "decode_us_avg": round(dec_avg_s * 1e6, 2),
+                     "decode_us_median": round(float(np.median(dec_ms)) * 1e3, 2)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3 / args.steps, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_info,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+# -------------------------------------------------------- reference arm --
+
+def run_reference(args, world: int, rank: int) -> dict | None:
+    """The float64 CPU oracle on the same workload, each step a bounded
+    prefix of the batch (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    from paged_kv_cache_249_gb300 import workload as wl
+    oracle.build()
+    w = wl.make(args.workload)
+    threads = os.cpu_count() or 1
+    step_budget = min(5.0, max(0.2, args.reference_seconds / max(1, args.steps + args.warmup)))
+    sub, n = _oracle_sample(w, step_budget, threads)
+    for _ in range(args.warmup):
+        _oracle_time(sub, w, threads)
+    times = [_oracle_time(sub, w, threads) for _ in range(args.steps)]
+    secs = float(np.sum(times))
+    kv = sub.kv_bytes_logical()
+    value = kv * args.steps / secs / 1e9
+    sample = (f"first {n} of {w.num_seqs} sequences per step ({kv / 1e9:.3f} GB of KV), "
+              f"float64 oracle on {threads} threads")
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), PCG64)", "impl": "reference",
+        "config": workload_config(w, args.workload, 1),
+        "seqs_per_s": round(n * args.steps / secs, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    from paged_kv_cache_249_gb300 import workload as wl
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--reference-seconds", type=float, default=120.0,
+                   help="CPU time budget of the whole reference arm")
+    p.add_argument("--json-out", default=None, help="also append the JSON line to this file")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    world, rank, _ = dist_setup(args.gpus)
+    line = run_reference(args, world, rank) if args.impl == "reference" else \
+        run_native(args, world, rank)
+    if line is not None:
+        text = json.dumps(line)
+        print(text, flush=True)
+        if args.json_out:
+            with open(args.json_out, "a") as f:
+                f.write(text + "\n")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

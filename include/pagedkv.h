@@ -1,0 +1,190 @@
+/*
+ * pagedkv.h -- C ABI of a paged KV-cache decode-attention library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the PagedAttention pages:
+ *   - the KV cache is cut into fixed-size blocks that need not be contiguous
+ *     in device memory (Qualiteg, "About PagedAttention for LLM serving",
+ *     section "1-2 ... divides the KV cache into blocks"; block sizes of
+ *     "around 16 to 256" are suggested there);
+ *   - logical blocks of a sequence map onto physical blocks through a block
+ *     table (same page, section "There are logical blocks and physical
+ *     blocks, and the two are linked by a block table");
+ *   - the cache grows by one token per iteration (same page, "Characteristics
+ *     of Autoregressive Models ..."), which pkv_reshape_and_cache writes;
+ *   - attention is computed over the non-contiguous blocks without padding
+ *     (same page, "[Regarding Problem 2] 2-1"; vAttention, section 3.1
+ *     "Requires re-writing the attention kernel", which also names the
+ *     grouped-query case), which pkv_paged_attention_decode computes.
+ *
+ * Conventions shared by every call
+ *   - Every device buffer is owned by the caller.  The library allocates no
+ *     device memory and keeps no mutable global state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work; nothing synchronises except
+ *     pkv_get_device_error.
+ *   - Invalid arguments are rejected on the host with PKV_ERR_INVALID_ARG or
+ *     PKV_ERR_UNSUPPORTED before anything is launched.  A failed launch
+ *     returns PKV_ERR_CUDA.  No C++ exception crosses this boundary.
+ *   - Data-dependent faults that only the device can see (a block-table
+ *     entry outside the pool, a slot past the pool, a context length beyond
+ *     the table) never trap: the kernel skips the bad work and ORs a
+ *     PKV_FAULT_* bit into the pool's error word, if one was given.
+ *   - All device pointers must be 16-byte aligned; the split-K workspace
+ *     must be 256-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, block_size, group, dtype */
+    PKV_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
+    PKV_ERR_WORKSPACE = 4,     /* split-K workspace missing or too small */
+    PKV_ERR_DEVICE_FAULT = 5   /* the device error word was non-zero */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits a kernel ORs into *pool->dev_error. */
+#define PKV_FAULT_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks): block skipped */
+#define PKV_FAULT_SLOT 2u      /* slot_mapping entry >= num_blocks*block_size: token skipped */
+#define PKV_FAULT_CONTEXT 4u   /* context_len < 0, > max_blocks_per_seq*block_size or
+                                  > max_context_len: clamped */
+#define PKV_FAULT_TIMEOUT 8u   /* a shared-memory pipeline wait ran past its bound */
+
+/* Flags of pkv_paged_attention_decode. */
+#define PKV_DECODE_PATH_AUTO 0  /* tensor cores when the GQA group makes dense tiles */
+#define PKV_DECODE_PATH_FMA 1   /* CUDA-core dot products for every group size */
+#define PKV_DECODE_PATH_MMA 2   /* tensor-core tiles (bf16 only) for every group size */
+
+/*
+ * Block pool: K and V are separate device buffers, each laid out
+ * [num_blocks][num_kv_heads][block_size][head_dim] row-major, so one
+ * (block, kv head) tile is block_size*head_dim contiguous elements and every
+ * row starts on a 16-byte boundary.  Filled by pkv_block_pool_init; treat as
+ * read-only afterwards.  `tma` holds the two TMA tensor descriptors (K, V)
+ * the decode kernel stages tiles with; it is only valid on `device`.
+ */
+typedef struct pkv_pool {
+    uint32_t magic;               /* set by pkv_block_pool_init; other values = not initialised */
+    int num_blocks;
+    int block_size;
+    int num_kv_heads;
+    int head_dim;
+    pkv_dtype dtype;
+    int device;
+    void *k_pool;
+    void *v_pool;
+    int32_t *dev_error;           /* device int32 or NULL */
+    uint64_t tma[32];             /* 2 x 128-byte descriptors, 64-byte aligned copy inside */
+} pkv_pool;
+
+/* Bytes of ONE pool (K or V): num_blocks*num_kv_heads*block_size*head_dim*elem. 0 if invalid. */
+size_t pkv_pool_bytes(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                      pkv_dtype dtype);
+
+/*
+ * Describe a caller-allocated block pool and prepare it for the kernels.
+ * k_pool/v_pool: device buffers of pkv_pool_bytes(...) bytes each, on the
+ * current device.  dev_error: device int32 error word or NULL.  zero_fill:
+ * non-zero clears both pools and the error word on `stream`.
+ * Supported: block_size in {16, 32}; head_dim in {64, 128}; dtype F32 or
+ * BF16; num_blocks*num_kv_heads*block_size < 2^31.
+ */
+pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, pkv_dtype dtype, void *k_pool, void *v_pool,
+                               int32_t *dev_error, int zero_fill, void *stream);
+
+/*
+ * Asynchronous host-to-device copy of a [num_seqs][max_blocks_per_seq] int32
+ * block table.  Entry (s, i) is the physical block of logical block i of
+ * sequence s; entries a sequence does not need may hold any value (-1 by
+ * convention).  If num_blocks > 0, every entry must be < num_blocks (negative
+ * = unused) or nothing is copied and PKV_ERR_INVALID_ARG is returned.  The
+ * host buffer must stay valid until the copy has run (pinned memory makes the
+ * copy truly asynchronous).
+ */
+pkv_status pkv_block_table_upload(int32_t *dev_block_tables, const int32_t *host_block_tables,
+                                  int num_seqs, int max_blocks_per_seq, int num_blocks,
+                                  void *stream);
+
+/*
+ * Cache write of the new tokens: for each t < num_tokens with
+ * slot = slot_mapping[t] >= 0, copy key[t][h][:] and value[t][h][:] to row
+ * slot % block_size of physical block slot / block_size, kv head h, for every
+ * h.  key/value: device [num_tokens][num_kv_heads][head_dim], pool dtype,
+ * contiguous.  slot_mapping: device int64 [num_tokens].  A negative slot is
+ * padding and skipped; a slot >= num_blocks*block_size sets PKV_FAULT_SLOT
+ * and is skipped.  Bytes are copied exactly.
+ */
+pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const void *value,
+                                 const int64_t *slot_mapping, int num_tokens, void *stream);
+
+/*
+ * Workspace bytes pkv_paged_attention_decode needs for split-K partials:
+ * num_seqs*num_heads*ceil(max_context_len/partition)*(head_dim+1)*4, rounded
+ * up to 256.  partition_tokens 0 (automatic) sizes for the smallest
+ * partition the automatic choice uses (512 tokens); -1 (never split) needs 0.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                  int partition_tokens);
+
+/*
+ * Decode-step attention of one new query token per sequence over its paged
+ * KV cache:
+ *   out[s][h][:] = sum_j softmax_j(scale * <query[s][h], K_s[j]>) V_s[j],
+ * j over logical positions 0 .. context_lens[s]-1, K_s[j]/V_s[j] the row of
+ * kv head h / (num_heads/num_kv_heads) in physical block
+ * block_tables[s][j / block_size], row j % block_size.  context_lens counts
+ * the new token, which pkv_reshape_and_cache must already have written.
+ * A sequence with context length 0 gets a zero row.
+ *
+ * query: device [num_seqs][num_heads][head_dim] in the pool dtype.
+ * out: device [num_seqs][num_heads][head_dim] in out_dtype (F32 or BF16).
+ * block_tables: device int32 [num_seqs][max_blocks_per_seq].
+ * context_lens: device int32 [num_seqs].
+ * max_context_len: host upper bound on every context length (grid sizing;
+ *   larger lengths are clamped and flagged PKV_FAULT_CONTEXT).
+ * partition_tokens: 0 = automatic, -1 = never split, > 0 = split every
+ *   sequence into partitions of this many tokens (a multiple of block_size,
+ *   at most 8192) and combine them with a log-sum-exp pass.
+ * workspace: device buffer of at least pkv_decode_workspace_bytes(...) bytes
+ *   when a split can happen (may be NULL with partition_tokens = -1).
+ * flags: one of PKV_DECODE_PATH_*.
+ * Supported groups: num_heads / num_kv_heads in 1..16.
+ */
+pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype out_dtype,
+                                      const void *query, int num_seqs, int num_heads,
+                                      int num_kv_heads, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *context_lens,
+                                      int max_context_len, float scale, int partition_tokens,
+                                      void *workspace, size_t workspace_bytes, int flags,
+                                      void *stream);
+
+/*
+ * Synchronise `stream`, read the pool's device error word into *fault_bits
+ * (may be NULL) and clear it.  Returns PKV_ERR_DEVICE_FAULT if it was
+ * non-zero, PKV_OK if zero or if the pool has no error word.
+ */
+pkv_status pkv_get_device_error(const pkv_pool *pool, void *stream, uint32_t *fault_bits);
+
+/* Static description of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Library ABI version (major*100 + minor). */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,116 @@
+// cache_and_combine.cu -- the cache-write scatter and the log-sum-exp combine
+// of a partitioned decode.
+#include <math_constants.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// ------------------------------------------------------ reshape_and_cache
+//
+// The KV cache grows by one token per decode iteration (Qualiteg, "About
+// PagedAttention for LLM serving", "Characteristics of Autoregressive
+// Models..."); the new token's K and V rows go to the slot its block table
+// assigns ("There are logical blocks and physical blocks...").  One thread
+// moves one 16-byte chunk of one (token, kv head) row of K and of V, so a
+// warp writes whole 128-byte lines of the destination row.
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
+                             const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                             const int64_t *__restrict__ slot_mapping, int num_tokens,
+                             int num_kv_heads, int block_size, int chunks_per_row,
+                             long long num_slots, int32_t *dev_error) {
+    const long long per_token = (long long)num_kv_heads * chunks_per_row;
+    const long long total = per_token * num_tokens;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(idx / per_token);
+        const int rem = (int)(idx - (long long)t * per_token);
+        const int h = rem / chunks_per_row, c = rem % chunks_per_row;
+        const long long slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;  // padding token
+        if (slot >= num_slots) {
+            if (rem == 0) raise_fault(dev_error, PKV_FAULT_SLOT);
+            continue;
+        }
+        const long long blk = slot / block_size, off = slot % block_size;
+        const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
+        const size_t src = (size_t)idx;  // key is [T][Hkv][D] contiguous
+        k_pool[dst] = __ldg(key + src);
+        v_pool[dst] = __ldg(value + src);
+    }
+}
+
+pkv_status launch_reshape_and_cache(const pkv_pool &pool, const void *key, const void *value,
+                                    const int64_t *slot_mapping, int num_tokens,
+                                    cudaStream_t stream) {
+    if (num_tokens == 0) return PKV_OK;
+    const int elem = pool.dtype == PKV_BF16 ? 2 : 4;
+    const int chunks = pool.head_dim * elem / 16;
+    const long long total = (long long)num_tokens * pool.num_kv_heads * chunks;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)sm_count(pool.device) * 8;
+    if (blocks > cap) blocks = cap;
+    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<uint4 *>(pool.k_pool), static_cast<uint4 *>(pool.v_pool),
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slot_mapping,
+        num_tokens, pool.num_kv_heads, pool.block_size, chunks,
+        (long long)pool.num_blocks * pool.block_size, pool.dev_error);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ lse_combine
+//
+// A context split into partitions p = 0..P-1 has, per query head, normalised
+// partial outputs o_p and their log2-sum-exp lse_p.  The full softmax result
+// is sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M) with M = max_p lse_p,
+// which is exact: the partitions' exponentials share one max-free total.
+__global__ void __launch_bounds__(128)
+    lse_combine_kernel(const DecodeArgs a, int head_dim, int block_size) {
+    __shared__ float red[4];
+    const int sh = blockIdx.x;  // s * H + h
+    const int s = sh / a.num_heads;
+    int ctx = __ldg(a.context_lens + s);
+    ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
+    const int nblk = (ctx + block_size - 1) / block_size;
+    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+    if (nparts <= 1) return;  // the decode kernel wrote this row directly
+    const float *lse = a.ws_lse + (size_t)sh * a.num_parts;
+    const float *po = a.ws_o + (size_t)sh * a.num_parts * head_dim;
+
+    float M = -CUDART_INF_F;
+    for (int p = threadIdx.x; p < nparts; p += blockDim.x) M = fmaxf(M, lse[p]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+
+    for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+        float num = 0.f, den = 0.f;
+        if (M != -CUDART_INF_F) {
+            for (int p = 0; p < nparts; ++p) {
+                const float w = fast_exp2(lse[p] - M);
+                den += w;
+                num = fmaf(w, po[(size_t)p * head_dim + d], num);
+            }
+        }
+        const float res = den > 0.f ? num / den : 0.f;
+        const size_t oi = (size_t)sh * head_dim + d;
+        if (a.out_bf16)
+            reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(res);
+        else
+            reinterpret_cast<float *>(a.out)[oi] = res;
+    }
+}
+
+pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, int block_size,
+                              cudaStream_t stream) {
+    const long long n = (long long)num_seqs * a.num_heads;
+    if (n == 0) return PKV_OK;
+    lse_combine_kernel<<<(unsigned)n, 128, 0, stream>>>(a, head_dim, block_size);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

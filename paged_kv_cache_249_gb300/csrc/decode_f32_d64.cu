@@ -1,0 +1,10 @@
+// decode_f32_d64.cu -- instantiations of the paged decode kernel for
+// f32 storage, head_dim 64 (one translation unit per combination so the
+// library builds in parallel).
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+pkv_status launch_decode_f32_d64(const DecodeLaunch &L) { return launch_d<float, 64>(L); }
+
+}  // namespace pkv

@@ -1,0 +1,628 @@
+// decode_kernel.cuh -- paged decode-attention kernel for sm_103a.
+//
+// One CTA computes the attention of the G query heads that share one KV head
+// (grouped-query attention, vAttention section 3.1) of one sequence over one
+// partition of its context.  The KV cache is read in place from the block
+// pool through the sequence's block table (Qualiteg, "There are logical
+// blocks and physical blocks, and the two are linked by a block table"), so
+// every (block, kv head) tile is read from HBM once per KV head, whatever G.
+//
+// Data movement: each warp owns NST shared-memory stages.  Lane 0 of the warp
+// stages a block's K and V tiles with 2-D TMA tiled copies (128-byte-wide
+// slabs, 128-byte swizzle) that complete on the stage's mbarrier; the warp
+// walks logical blocks warp, warp+NW, warp+2NW, ... of the partition.  Block
+// numbers are gathered 32 at a time by the whole warp, one chunk ahead.
+//
+// Arithmetic (standard softmax attention, online form): scores in the log2
+// domain, a running max m and sum l per query row, the accumulator rescaled
+// by 2^(m_old - m_new) whenever the max grows.  Two compute paths:
+//   * FMA: CUDA-core dot products; a row of D elements is spread over
+//     LPT lanes (16-byte chunks), reduced with xor shuffles.
+//   * MMA: bf16 mma.sync m16n8k16 with the G query rows padded to 16:
+//     S = Q K^T per block from ldmatrix'd K, then O += P V with P split into
+//     a bf16 high part and a bf16 remainder so the weights keep ~16 bits.
+// At the end the per-warp states are merged with a log-sum-exp combine in
+// shared memory; a partitioned (split) context writes normalised partials
+// and their log2-sum-exp, which lse_combine reduces.
+#pragma once
+
+#include <math_constants.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+template <typename T>
+struct ElemTraits;
+template <>
+struct ElemTraits<float> {
+    static constexpr int kBytes = 4;
+};
+template <>
+struct ElemTraits<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+};
+
+template <typename T, int D, int BS>
+struct Geom {
+    static constexpr int kElemBytes = ElemTraits<T>::kBytes;
+    static constexpr int kRowBytes = D * kElemBytes;
+    static constexpr int kSlabs = kRowBytes / 128;      // 128-byte-wide column slabs
+    static constexpr int kSlabElems = 128 / kElemBytes;
+    static constexpr int kSlabBytes = BS * 128;
+    static constexpr int kTileBytes = BS * kRowBytes;   // one (block, kv head) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
+    static constexpr int kChunks = kRowBytes / 16;      // 16-byte chunks per row
+    static constexpr int kEPC = 16 / kElemBytes;        // elements per chunk
+    static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte slabs");
+};
+
+constexpr int kDecodeWarps = 4;
+
+template <typename T, int D, int BS>
+constexpr int decode_stages() {
+    constexpr int per = kDecodeWarps * Geom<T, D, BS>::kStageBytes;
+    constexpr int n = 98304 / per;
+    return n < 1 ? 1 : (n > 6 ? 6 : n);
+}
+
+template <typename T, int D, int BS>
+constexpr int decode_smem_bytes() {
+    // stages + one mbarrier per stage + slack to align the base to 1024 bytes
+    return kDecodeWarps * decode_stages<T, D, BS>() * Geom<T, D, BS>::kStageBytes +
+           kDecodeWarps * decode_stages<T, D, BS>() * 8 + 1024;
+}
+
+// Per-warp state exported for the cross-warp merge: m[GP], l[GP], o[GP][D].
+template <int GP, int D>
+struct WarpState {
+    float m[GP];
+    float l[GP];
+    float o[GP][D];
+};
+
+__device__ __forceinline__ float load_as_float(const float *p) { return *p; }
+__device__ __forceinline__ float load_as_float(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+
+// Load 16 bytes of q / K / V and widen to EPC floats.
+template <typename T>
+__device__ __forceinline__ void widen16(const uint4 &v, float *f);
+template <>
+__device__ __forceinline__ void widen16<float>(const uint4 &v, float *f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ __forceinline__ void widen16<__nv_bfloat16>(const uint4 &v, float *f) {
+    f[0] = bf16_lo(v.x);
+    f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y);
+    f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z);
+    f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w);
+    f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// ------------------------------------------------------------ FMA compute
+
+template <typename T, int D, int BS, int GP>
+struct FmaPath {
+    using Gm = Geom<T, D, BS>;
+    static constexpr int LPT = Gm::kChunks < 16 ? Gm::kChunks : 16;  // lanes per token
+    static constexpr int CPL = Gm::kChunks / LPT;                    // chunks per lane
+    static constexpr int TPP = 32 / LPT;                             // tokens per pass
+    static constexpr int NI = BS / TPP;                              // passes per block
+    static constexpr int EPC = Gm::kEPC;
+
+    float q[GP][CPL][EPC];  // query rows, pre-multiplied by scale*log2(e)
+    float m[GP], l[GP];
+    float acc[GP][CPL][EPC];
+    int tg, li;
+
+    __device__ __forceinline__ void init(const T *qrow0, int group, float scale_log2, int lane) {
+        tg = lane / LPT;
+        li = lane % LPT;
+#pragma unroll
+        for (int r = 0; r < GP; ++r) {
+            m[r] = -CUDART_INF_F;
+            l[r] = 0.f;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                float f[EPC];
+                if (r < group) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const char *>(qrow0 + (size_t)r * D) + (li + k * LPT) * 16);
+                    widen16<T>(v, f);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) f[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) {
+                    q[r][k][e] = f[e] * scale_log2;
+                    acc[r][k][e] = 0.f;
+                }
+            }
+        }
+    }
+
+    // One staged block: K tile at kaddr, V tile at vaddr (shared addresses),
+    // the first `nvalid` of its BS rows are context tokens.
+    __device__ __forceinline__ void block(uint32_t kaddr, uint32_t vaddr, int nvalid) {
+        float sc[NI][GP];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int tok = tg + i * TPP;
+            float part[GP];
+#pragma unroll
+            for (int r = 0; r < GP; ++r) part[r] = 0.f;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                float kf[EPC];
+                widen16<T>(lds128(kaddr + swz_offset<BS>(tok, li + k * LPT)), kf);
+#pragma unroll
+                for (int r = 0; r < GP; ++r)
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) part[r] = fmaf(q[r][k][e], kf[e], part[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < GP; ++r) {
+#pragma unroll
+                for (int off = LPT / 2; off > 0; off >>= 1)
+                    part[r] += __shfl_xor_sync(0xffffffffu, part[r], off);
+                sc[i][r] = tok < nvalid ? part[r] : -CUDART_INF_F;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < GP; ++r) {
+            float mx = sc[0][r];
+#pragma unroll
+            for (int i = 1; i < NI; ++i) mx = fmaxf(mx, sc[i][r]);
+            const float mn = fmaxf(m[r], mx);
+            const float mu = mn == -CUDART_INF_F ? 0.f : mn;
+            const float alpha = fast_exp2(m[r] - mu);
+            m[r] = mn;
+            float lsum = l[r] * alpha;
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                sc[i][r] = fast_exp2(sc[i][r] - mu);
+                lsum += sc[i][r];
+            }
+            l[r] = lsum;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[r][k][e] *= alpha;
+        }
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int tok = tg + i * TPP;
+            if (tok < nvalid) {  // masked rows may hold stale bits (even NaN): never touch them
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) {
+                    float vf[EPC];
+                    widen16<T>(lds128(vaddr + swz_offset<BS>(tok, li + k * LPT)), vf);
+#pragma unroll
+                    for (int r = 0; r < GP; ++r)
+#pragma unroll
+                        for (int e = 0; e < EPC; ++e) acc[r][k][e] = fmaf(sc[i][r], vf[e], acc[r][k][e]);
+                }
+            }
+        }
+    }
+
+    // Merge the TPP token streams of the warp and write the warp's state.
+    __device__ __forceinline__ void finish(WarpState<GP, D> *st, int lane) {
+#pragma unroll
+        for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+            for (int r = 0; r < GP; ++r) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[r], off);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[r], off);
+                const float mn = fmaxf(m[r], mo);
+                const float mu = mn == -CUDART_INF_F ? 0.f : mn;
+                const float wa = fast_exp2(m[r] - mu), wb = fast_exp2(mo - mu);
+                l[r] = l[r] * wa + lo * wb;
+                m[r] = mn;
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) {
+                        const float ao = __shfl_xor_sync(0xffffffffu, acc[r][k][e], off);
+                        acc[r][k][e] = acc[r][k][e] * wa + ao * wb;
+                    }
+            }
+        }
+        if (lane < LPT) {
+#pragma unroll
+            for (int r = 0; r < GP; ++r) {
+#pragma unroll
+                for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) st->o[r][(li + k * LPT) * EPC + e] = acc[r][k][e];
+                if (lane == 0) {
+                    st->m[r] = m[r];
+                    st->l[r] = l[r];
+                }
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------ MMA compute
+
+template <int D, int BS>
+struct MmaPath {
+    using T = __nv_bfloat16;
+    static constexpr int GP = 16;
+    static constexpr int KS = D / 16;   // k-steps of the QK^T product
+    static constexpr int NT = BS / 8;   // token n-tiles per block
+    static constexpr int ND = D / 8;    // head-dim n-tiles of the PV product
+    static_assert(BS % 16 == 0 && D % 32 == 0, "tile shape");
+
+    uint32_t qa[KS][4];                 // A fragments of Q (rows g, g+8)
+    float o[ND][4];                     // O accumulators (rows g, g+8)
+    float m0, m1, l0, l1;               // rows g and g+8; l is lane-partial
+    float scale_log2;
+    int gid, tig;
+
+    __device__ __forceinline__ void init(const T *qrow0, int group, float sl2, int lane) {
+        gid = lane >> 2;
+        tig = lane & 3;
+        scale_log2 = sl2;
+        m0 = m1 = -CUDART_INF_F;
+        l0 = l1 = 0.f;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow0);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int c0 = (ks * 16 + 2 * tig) / 2, c1 = (ks * 16 + 8 + 2 * tig) / 2;
+            qa[ks][0] = gid < group ? __ldg(q32 + (size_t)gid * (D / 2) + c0) : 0u;
+            qa[ks][1] = gid + 8 < group ? __ldg(q32 + (size_t)(gid + 8) * (D / 2) + c0) : 0u;
+            qa[ks][2] = gid < group ? __ldg(q32 + (size_t)gid * (D / 2) + c1) : 0u;
+            qa[ks][3] = gid + 8 < group ? __ldg(q32 + (size_t)(gid + 8) * (D / 2) + c1) : 0u;
+        }
+#pragma unroll
+        for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t kaddr, uint32_t vaddr, int nvalid, int lane) {
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            const int row = nt * 8 + (lane & 7);
+#pragma unroll
+            for (int kc = 0; kc < D / 32; ++kc) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kaddr + swz_offset<BS>(row, kc * 4 + (lane >> 3)), b0, b1, b2, b3);
+                mma_bf16_16816(s[nt], qa[2 * kc], b0, b1);
+                mma_bf16_16816(s[nt], qa[2 * kc + 1], b2, b3);
+            }
+        }
+        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const bool ok = nt * 8 + 2 * tig + e < nvalid;
+                s[nt][e] = ok ? s[nt][e] * scale_log2 : -CUDART_INF_F;
+                s[nt][2 + e] = ok ? s[nt][2 + e] * scale_log2 : -CUDART_INF_F;
+                mx0 = fmaxf(mx0, s[nt][e]);
+                mx1 = fmaxf(mx1, s[nt][2 + e]);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+        const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+        const float a0 = fast_exp2(m0 - mu0), a1 = fast_exp2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                s[nt][e] = fast_exp2(s[nt][e] - mu0);
+                s[nt][2 + e] = fast_exp2(s[nt][2 + e] - mu1);
+                ls0 += s[nt][e];
+                ls1 += s[nt][2 + e];
+            }
+        }
+        l0 = l0 * a0 + ls0;
+        l1 = l1 * a1 + ls1;
+#pragma unroll
+        for (int n = 0; n < ND; ++n) {
+            o[n][0] *= a0;
+            o[n][1] *= a0;
+            o[n][2] *= a1;
+            o[n][3] *= a1;
+        }
+#pragma unroll
+        for (int kt = 0; kt < BS / 16; ++kt) {
+            // P as A fragments: high bf16 part and the bf16 of the remainder
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float *sv = s[2 * kt + j];
+                ph[2 * j] = pack_bf16(sv[0], sv[1]);
+                ph[2 * j + 1] = pack_bf16(sv[2], sv[3]);
+                pl[2 * j] = pack_bf16(sv[0] - bf16_lo(ph[2 * j]), sv[1] - bf16_hi(ph[2 * j]));
+                pl[2 * j + 1] =
+                    pack_bf16(sv[2] - bf16_lo(ph[2 * j + 1]), sv[3] - bf16_hi(ph[2 * j + 1]));
+            }
+            const bool partial = nvalid < (kt + 1) * 16;
+            const int t0 = kt * 16 + 2 * tig;
+            const uint32_t mlo = (partial ? (t0 < nvalid ? 0x0000ffffu : 0u) |
+                                                (t0 + 1 < nvalid ? 0xffff0000u : 0u)
+                                          : 0xffffffffu);
+            const uint32_t mhi = (partial ? (t0 + 8 < nvalid ? 0x0000ffffu : 0u) |
+                                                (t0 + 9 < nvalid ? 0xffff0000u : 0u)
+                                          : 0xffffffffu);
+            const int tok = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int np = 0; np < ND / 2; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vaddr + swz_offset<BS>(tok, np * 2 + (lane >> 4)), b0, b1, b2, b3);
+                // rows past the context may hold stale bits (even NaN): zero them
+                b0 &= mlo;
+                b2 &= mlo;
+                b1 &= mhi;
+                b3 &= mhi;
+                mma_bf16_16816(o[2 * np], ph, b0, b1);
+                mma_bf16_16816(o[2 * np], pl, b0, b1);
+                mma_bf16_16816(o[2 * np + 1], ph, b2, b3);
+                mma_bf16_16816(o[2 * np + 1], pl, b2, b3);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish(WarpState<GP, D> *st, int lane) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+        for (int n = 0; n < ND; ++n) {
+            const int d = n * 8 + 2 * tig;
+            st->o[gid][d] = o[n][0];
+            st->o[gid][d + 1] = o[n][1];
+            st->o[gid + 8][d] = o[n][2];
+            st->o[gid + 8][d + 1] = o[n][3];
+        }
+        if (tig == 0) {
+            st->m[gid] = m0;
+            st->m[gid + 8] = m1;
+            st->l[gid] = l0;
+            st->l[gid + 8] = l1;
+        }
+    }
+};
+
+// ------------------------------------------------------------------ kernel
+
+template <typename T, int D, int BS, int GP, bool MMA>
+struct PathOf {
+    using type = FmaPath<T, D, BS, GP>;
+};
+template <int D, int BS, int GP>
+struct PathOf<__nv_bfloat16, D, BS, GP, true> {
+    using type = MmaPath<D, BS>;
+};
+
+template <typename T, int D, int BS, int GP, bool MMA>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
+    using Gm = Geom<T, D, BS>;
+    using Path = typename PathOf<T, D, BS, GP, MMA>::type;
+    constexpr int NW = kDecodeWarps;
+    constexpr int NST = decode_stages<T, D, BS>();
+    constexpr int RG = MMA ? 16 : GP;  // rows of the exported warp state
+    static_assert(sizeof(WarpState<RG, D>) <= NST * Gm::kStageBytes, "state fits in stages");
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int s = blockIdx.x, g = blockIdx.y, part = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int ctx = __ldg(a.context_lens + s);
+    if (ctx < 0 || ctx > a.ctx_cap) {
+        if (threadIdx.x == 0 && g == 0 && part == 0) raise_fault(a.dev_error, PKV_FAULT_CONTEXT);
+        ctx = ctx < 0 ? 0 : a.ctx_cap;
+    }
+    const int nblk = (ctx + BS - 1) / BS;
+    const int b0 = part * a.part_blocks;
+    if (part > 0 && b0 >= nblk) return;  // the sequence has no such partition
+    const int b1 = min(nblk, b0 + a.part_blocks);
+    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+
+    unsigned char *wstage = smem + warp * NST * Gm::kStageBytes;
+    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + NW * NST * Gm::kStageBytes) + warp * NST;
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < NST; ++i) mbar_init(&wbar[i], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    __syncwarp();
+
+    // this warp's logical blocks: b0 + warp + i*NW, i < nw
+    const int span = b1 - b0;
+    const int nw = span > warp ? (span - warp + NW - 1) / NW : 0;
+    const int32_t *bt_row = a.block_tables + (size_t)s * a.max_blocks_per_seq;
+    auto bt_load = [&](int chunk) -> int {
+        const int i = chunk * 32 + lane;
+        return i < nw ? __ldg(bt_row + b0 + warp + i * NW) : -1;
+    };
+    int ent0 = bt_load(0), ent1 = bt_load(1);
+    int cb = 0;  // chunk held in ent0
+    auto bt_get = [&](int i) -> int {
+        const int v0 = __shfl_sync(0xffffffffu, ent0, i & 31);
+        const int v1 = __shfl_sync(0xffffffffu, ent1, i & 31);
+        return (i >> 5) == cb ? v0 : v1;
+    };
+    auto issue = [&](int i, int pb) {
+        if (lane == 0) {
+            uint64_t *bar = &wbar[i % NST];
+            if (pb >= 0 && pb < a.num_blocks) {
+                mbar_arrive_expect_tx(bar, Gm::kStageBytes);
+                unsigned char *dk = wstage + (i % NST) * Gm::kStageBytes;
+                unsigned char *dv = dk + Gm::kTileBytes;
+                const int y = (pb * a.num_kv_heads + g) * BS;
+#pragma unroll
+                for (int sl = 0; sl < Gm::kSlabs; ++sl) {
+                    tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);
+                    tma_load_2d(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar);
+                }
+            } else {
+                raise_fault(a.dev_error, PKV_FAULT_BLOCK_ID);
+                mbar_arrive(bar);
+            }
+        }
+    };
+
+    Path path;
+    const T *qrow0 = reinterpret_cast<const T *>(a.q) +
+                     ((size_t)s * a.num_heads + (size_t)g * a.group) * D;
+    path.init(qrow0, a.group, a.scale_log2, lane);
+
+#pragma unroll 1
+    for (int i = 0; i < NST && i < nw; ++i) issue(i, bt_get(i));
+
+    int i = 0;
+    bool ok = true;
+#pragma unroll 1
+    for (; i < nw; ++i) {
+        if ((i >> 5) != cb) {
+            cb = i >> 5;
+            ent0 = ent1;
+            ent1 = bt_load(cb + 1);
+        }
+        const int pb = bt_get(i);
+        ok = __all_sync(0xffffffffu, mbar_wait(&wbar[i % NST], (i / NST) & 1));
+        if (!ok) break;
+        if (pb >= 0 && pb < a.num_blocks) {
+            const int lblk = b0 + warp + i * NW;
+            const int nvalid = min(BS, ctx - lblk * BS);
+            const uint32_t kaddr = smem_u32(wstage + (i % NST) * Gm::kStageBytes);
+            if constexpr (MMA)
+                path.block(kaddr, kaddr + Gm::kTileBytes, nvalid, lane);
+            else
+                path.block(kaddr, kaddr + Gm::kTileBytes, nvalid);
+        }
+        __syncwarp();
+        if (i + NST < nw) issue(i + NST, bt_get(i + NST));
+    }
+    if (!ok) {
+        if (lane == 0) raise_fault(a.dev_error, PKV_FAULT_TIMEOUT);
+        // drain what this warp still has in flight, again with a bound
+        for (int j = i; j < nw && j < i + NST; ++j) mbar_wait(&wbar[j % NST], (j / NST) & 1);
+    }
+
+    // ---- merge the warps' states (each warp reuses its own stages)
+    WarpState<RG, D> *st = reinterpret_cast<WarpState<RG, D> *>(wstage);
+    path.finish(st, lane);
+    __syncthreads();
+
+    const int G = a.group;
+    const bool split = nparts > 1;
+    const size_t head0 = (size_t)s * a.num_heads + (size_t)g * G;
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int r = idx / D, d = idx % D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            M = fmaxf(M, reinterpret_cast<WarpState<RG, D> *>(smem + w * NST * Gm::kStageBytes)->m[r]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const WarpState<RG, D> *ws =
+                    reinterpret_cast<const WarpState<RG, D> *>(smem + w * NST * Gm::kStageBytes);
+                const float f = fast_exp2(ws->m[r] - M);
+                L += ws->l[r] * f;
+                O += ws->o[r][d] * f;
+            }
+        }
+        const float res = L > 0.f ? O / L : 0.f;
+        if (!split) {
+            const size_t oi = (head0 + r) * D + d;
+            if (a.out_bf16)
+                reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(res);
+            else
+                reinterpret_cast<float *>(a.out)[oi] = res;
+        } else {
+            const size_t pi = (head0 + r) * a.num_parts + part;
+            a.ws_o[pi * D + d] = res;
+            if (d == 0) a.ws_lse[pi] = L > 0.f ? M + __log2f(L) : -CUDART_INF_F;
+        }
+    }
+}
+
+// Explicit-instantiation helper: launch one configuration.
+template <typename T, int D, int BS, int GP, bool MMA>
+pkv_status launch_one(const DecodeLaunch &L) {
+    auto kern = paged_decode_kernel<T, D, BS, GP, MMA>;
+    constexpr int smem = decode_smem_bytes<T, D, BS>();
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    // Raise the dynamic shared-memory limit once per device for this kernel.
+    static unsigned long long done_mask = 0ull;
+    const unsigned long long bit = 1ull << (L.device & 63);
+    if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
+    }
+    dim3 grid(L.num_seqs, L.args.num_kv_heads, L.args.num_parts);
+    kern<<<grid, kDecodeWarps * 32, smem, L.stream>>>(*L.tmk, *L.tmv, L.args);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <typename T, int D, int BS>
+pkv_status launch_bs(const DecodeLaunch &L) {
+    if constexpr (sizeof(T) == 2) {
+        if (L.mma) return launch_one<T, D, BS, 16, true>(L);
+    }
+    switch (L.group_pad) {
+        case 1: return launch_one<T, D, BS, 1, false>(L);
+        case 2: return launch_one<T, D, BS, 2, false>(L);
+        case 4: return launch_one<T, D, BS, 4, false>(L);
+        case 8: return launch_one<T, D, BS, 8, false>(L);
+        case 16: return launch_one<T, D, BS, 16, false>(L);
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename T, int D>
+pkv_status launch_d(const DecodeLaunch &L) {
+    switch (L.block_size) {
+        case 16: return launch_bs<T, D, 16>(L);
+        case 32: return launch_bs<T, D, 32>(L);
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace pkv

@@ -1,0 +1,243 @@
+"""Thin ctypes binding over libpagedkv.so (the C ABI of include/pagedkv.h).
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing or was built
+for another machine, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+# pkv_status
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_FAULT = range(6)
+# pkv_dtype
+F32, BF16 = 0, 1
+# device fault bits
+FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT = 1, 2, 4, 8
+# decode paths
+PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
+
+EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
+           "pkv_reshape_and_cache", "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
+           "pkv_get_device_error", "pkv_status_string", "pkv_version"]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class pkv_pool(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint32), ("num_blocks", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("device", ctypes.c_int),
+                ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("dev_error", ctypes.c_void_p), ("tma", ctypes.c_uint64 * 32)]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libpagedkv.so and declare its signatures (raises if absent)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with paged_kv_cache_249_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    I, P, Z, F = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+    PP = ctypes.POINTER(pkv_pool)
+    sig = {
+        "pkv_pool_bytes": (Z, [I, I, I, I, I]),
+        "pkv_block_pool_init": (I, [PP, I, I, I, I, I, P, P, P, I, P]),
+        "pkv_block_table_upload": (I, [P, P, I, I, I, P]),
+        "pkv_reshape_and_cache": (I, [PP, P, P, P, I, P]),
+        "pkv_decode_workspace_bytes": (Z, [I, I, I, I, I]),
+        "pkv_paged_attention_decode": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, P, Z, I, P]),
+        "pkv_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
+        "pkv_status_string": (ctypes.c_char_p, [I]),
+        "pkv_version": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise PagedKVError(status, where)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def pool_bytes(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+               dtype: torch.dtype) -> int:
+    return load().pkv_pool_bytes(num_blocks, block_size, num_kv_heads, head_dim, _dtype_code(dtype))
+
+
+class BlockPool:
+    """A caller-owned K/V block pool described to the library."""
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                 dev_error: Optional[torch.Tensor] = None, zero_fill: bool = False,
+                 stream: Optional[torch.cuda.Stream] = None):
+        assert k_pool.shape == v_pool.shape and k_pool.dtype == v_pool.dtype
+        assert k_pool.is_contiguous() and v_pool.is_contiguous()
+        NB, Hkv, BS, D = k_pool.shape
+        self.k_pool, self.v_pool, self.dev_error = k_pool, v_pool, dev_error
+        self.desc = pkv_pool()
+        _check(load().pkv_block_pool_init(ctypes.byref(self.desc), NB, BS, Hkv, D,
+                                          _dtype_code(k_pool.dtype), k_pool.data_ptr(),
+                                          v_pool.data_ptr(), _ptr(dev_error), int(zero_fill),
+                                          _stream(stream)), "pkv_block_pool_init")
+
+    @property
+    def num_blocks(self) -> int:
+        return self.desc.num_blocks
+
+    @property
+    def block_size(self) -> int:
+        return self.desc.block_size
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.desc.num_kv_heads
+
+    @property
+    def head_dim(self) -> int:
+        return self.desc.head_dim
+
+
+def block_pool_init(k_pool, v_pool, dev_error=None, zero_fill=False, stream=None) -> BlockPool:
+    return BlockPool(k_pool, v_pool, dev_error, zero_fill, stream)
+
+
+def block_table_upload(dev_block_tables: torch.Tensor, host_block_tables: torch.Tensor,
+                       num_blocks: int = 0, stream=None) -> None:
+    """Asynchronous H2D copy of an int32 [S][max_blocks] table (host tensor
+    should be pinned and must stay alive until the copy has run)."""
+    assert host_block_tables.dtype == torch.int32 and host_block_tables.is_contiguous()
+    assert dev_block_tables.dtype == torch.int32 and dev_block_tables.is_contiguous()
+    S, MB = host_block_tables.shape
+    assert tuple(dev_block_tables.shape) == (S, MB)
+    _check(load().pkv_block_table_upload(dev_block_tables.data_ptr(), host_block_tables.data_ptr(),
+                                         S, MB, num_blocks, _stream(stream)),
+           "pkv_block_table_upload")
+
+
+def reshape_and_cache(pool: BlockPool, key: torch.Tensor, value: torch.Tensor,
+                      slot_mapping: torch.Tensor, stream=None) -> None:
+    assert slot_mapping.dtype == torch.int64
+    _check(load().pkv_reshape_and_cache(ctypes.byref(pool.desc), key.data_ptr(), value.data_ptr(),
+                                        slot_mapping.data_ptr(), slot_mapping.numel(),
+                                        _stream(stream)), "pkv_reshape_and_cache")
+
+
+def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                           partition_tokens: int = 0) -> int:
+    return load().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len,
+                                             partition_tokens)
+
+
+def paged_attention_decode(pool: BlockPool, out: torch.Tensor, query: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           max_context_len: int, scale: float, num_kv_heads: Optional[int] = None,
+                           partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                           path: int = PATH_AUTO, stream=None) -> None:
+    S, H, _ = query.shape
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_paged_attention_decode(
+        ctypes.byref(pool.desc), out.data_ptr(), _dtype_code(out.dtype), query.data_ptr(), S, H,
+        num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), int(max_context_len), float(scale),
+        int(partition_tokens), _ptr(workspace), ws_bytes, int(path), _stream(stream)),
+        "pkv_paged_attention_decode")
+
+
+def get_device_error(pool: BlockPool, stream=None) -> int:
+    """Synchronise, return and clear the pool's device fault bits."""
+    bits = ctypes.c_uint32(0)
+    st = load().pkv_get_device_error(ctypes.byref(pool.desc), _stream(stream), ctypes.byref(bits))
+    if st not in (OK, ERR_DEVICE_FAULT):
+        _check(st, "pkv_get_device_error")
+    return int(bits.value)
+
+
+def alloc_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                    partition_tokens: int = 0, device=None) -> Optional[torch.Tensor]:
+    """A torch-owned workspace buffer of the size the library asks for."""
+    n = decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+class DeviceWorkload:
+    """A Workload's tensors resident on the GPU, with its pool described."""
+
+    def __init__(self, w, device="cuda", out_dtype: Optional[torch.dtype] = None,
+                 partition_tokens: Optional[int] = None):
+        self.w = w
+        self.q = w.q.to(device)
+        self.k_pool = w.k_pool.to(device)
+        self.v_pool = w.v_pool.to(device)
+        self.new_key = w.new_key.to(device)
+        self.new_value = w.new_value.to(device)
+        self.block_tables = torch.from_numpy(w.block_tables).to(device)
+        self.context_lens = torch.from_numpy(w.context_lens).to(device)
+        self.slot_mapping = torch.from_numpy(w.slot_mapping).to(device)
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=device)
+        self.pool = BlockPool(self.k_pool, self.v_pool, self.dev_error)
+        self.out = torch.empty(w.num_seqs, w.num_heads, w.head_dim,
+                               dtype=out_dtype or torch.float32, device=device)
+        self.partition_tokens = w.partition_tokens if partition_tokens is None else partition_tokens
+        self.max_context_len = max(1, w.max_context_len)
+        self.workspace = alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, self.max_context_len,
+                                         self.partition_tokens, device)
+
+    def step(self, path: int = PATH_AUTO, stream=None) -> None:
+        """One decode step: cache write of the new tokens, then attention."""
+        reshape_and_cache(self.pool, self.new_key, self.new_value, self.slot_mapping, stream)
+        self.decode(path=path, stream=stream)
+
+    def decode(self, path: int = PATH_AUTO, stream=None) -> None:
+        paged_attention_decode(self.pool, self.out, self.q, self.block_tables, self.context_lens,
+                               self.max_context_len, self.w.scale, self.w.num_kv_heads,
+                               self.partition_tokens, self.workspace, path, stream)

@@ -1,0 +1,131 @@
+"""Element-by-element parity of the CUDA path with the float64 oracle.
+
+Cache writes are compared byte for byte over the whole pool; attention
+outputs within 1e-5 (fp32 inputs) or 2e-3 (bf16 inputs, fp32 accumulation),
+on sizes that span several tiles, partitions and a ragged last block.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_249_gb300 import pagedkv, workload
+from tests.gpu_helpers import assert_close, oracle_after_write, run_decode
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 15, 16, 17, 100, 333, 700]
+
+
+def _w(dtype, D, BS, H, Hkv, ctx=RAGGED, seed=0, **kw):
+    return workload.build(f"parity_{dtype}_d{D}_bs{BS}_h{H}_{Hkv}", dtype=dtype, context_lens=ctx,
+                          num_heads=H, num_kv_heads=Hkv, head_dim=D, block_size=BS,
+                          data_seed=1000 + seed, meta_seed=2000 + seed, **kw)
+
+
+# ------------------------------------------------------------ cache write --
+
+@pytest.mark.parametrize("dtype,D,BS", [("f32", 64, 16), ("bf16", 128, 16), ("bf16", 64, 32),
+                                        ("f32", 128, 32)])
+def test_reshape_and_cache_bit_exact(dtype, D, BS):
+    w = _w(dtype, D, BS, 8, 4, ctx=[1, 16, 17, 40, 64, 65], pool_blocks=30)
+    sm = w.slot_mapping.copy()
+    sm[1] = -1                          # padding token: skipped
+    dw = pagedkv.DeviceWorkload(w)
+    dw.slot_mapping.copy_(torch.from_numpy(sm))
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw.pool) == 0
+    kp, vp = w.k_pool.clone(), w.v_pool.clone()
+    assert oracle.reshape_and_cache(kp, vp, w.new_key, w.new_value, sm) == 0
+    view = torch.int32 if dtype == "f32" else torch.int16
+    assert torch.equal(dw.k_pool.cpu().view(view), kp.view(view))
+    assert torch.equal(dw.v_pool.cpu().view(view), vp.view(view))
+
+
+def test_reshape_and_cache_slot_past_pool_faults_and_skips():
+    w = _w("bf16", 128, 16, 8, 2, ctx=[5, 20, 33])
+    sm = w.slot_mapping.copy()
+    sm[2] = w.num_blocks * w.block_size  # one past the last slot
+    dw = pagedkv.DeviceWorkload(w)
+    dw.slot_mapping.copy_(torch.from_numpy(sm))
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    assert pagedkv.get_device_error(dw.pool) == pagedkv.FAULT_SLOT
+    kp, vp = w.k_pool.clone(), w.v_pool.clone()
+    assert oracle.reshape_and_cache(kp, vp, w.new_key, w.new_value, sm) == 1
+    assert torch.equal(dw.k_pool.cpu().view(torch.int16), kp.view(torch.int16))
+    assert torch.equal(dw.v_pool.cpu().view(torch.int16), vp.view(torch.int16))
+
+
+# ---------------------------------------------------------------- decode --
+
+CASES = [
+    # dtype, D, BS, H, Hkv
+    ("f32", 64, 16, 4, 4),
+    ("f32", 128, 16, 8, 2),
+    ("f32", 64, 32, 12, 4),
+    ("f32", 128, 32, 16, 1),
+    ("bf16", 128, 16, 32, 32),
+    ("bf16", 128, 16, 32, 8),
+    ("bf16", 128, 16, 64, 8),
+    ("bf16", 64, 16, 8, 4),
+    ("bf16", 64, 32, 12, 4),
+    ("bf16", 128, 32, 16, 1),
+    ("bf16", 128, 16, 6, 2),
+]
+
+
+@pytest.mark.parametrize("partition", [-1, 0, 64])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "_".join(map(str, c)))
+def test_decode_matches_oracle(case, partition):
+    dtype, D, BS, H, Hkv = case
+    w = _w(dtype, D, BS, H, Hkv, seed=CASES.index(case))
+    ref, _, _ = oracle_after_write(w)
+    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_FMA] + ([pagedkv.PATH_MMA] if dtype == "bf16" else [])
+    for path in paths:
+        dw = run_decode(w, path=path, partition_tokens=partition)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, dtype, f"{case} path={path} partition={partition}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bf16_output(dtype):
+    w = _w(dtype, 128, 16, 16, 4, seed=5)
+    ref, _, _ = oracle_after_write(w)
+    dw = run_decode(w, partition_tokens=128, out_dtype=torch.bfloat16)
+    assert_close(dw.out, ref, dtype, "bf16 output")
+
+
+def test_tiny_f32_workload():
+    w = workload.make("tiny_f32")
+    ref, _, _ = oracle_after_write(w)
+    dw = run_decode(w)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "f32", "tiny_f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_long_context_many_partitions(dtype):
+    w = _w(dtype, 128, 16, 16, 2, ctx=[9000, 4097, 1, 513], seed=9)
+    ref, _, _ = oracle_after_write(w)
+    for pt in (-1, 0, 512, 2048):
+        dw = run_decode(w, partition_tokens=pt)
+        assert_close(dw.out, ref, dtype, f"partition {pt}")
+
+
+def test_random_shapes_sweep():
+    rng = np.random.default_rng(77)
+    for trial in range(12):
+        dtype = ["f32", "bf16"][trial % 2]
+        D = [64, 128][(trial // 2) % 2]
+        BS = [16, 32][(trial // 4) % 2]
+        Hkv = int(rng.integers(1, 5))
+        G = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+        S = int(rng.integers(1, 9))
+        ctx = rng.integers(0, 1500, size=S).tolist()
+        w = _w(dtype, D, BS, Hkv * G, Hkv, ctx=ctx, seed=300 + trial)
+        ref, _, _ = oracle_after_write(w)
+        pt = int(rng.choice([-1, 0, BS * 4, BS * 16]))
+        dw = run_decode(w, partition_tokens=pt)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, dtype, f"trial {trial}: {dtype} D{D} BS{BS} G{G} ctx {ctx} pt {pt}")
