@@ -170,6 +170,41 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
                                       void *workspace, size_t workspace_bytes, int flags,
                                       void *stream);
 
+/* Size of the fixed split-K scratch array behind pkv_paged_attention_decode_static. */
+#define PKV_STATIC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * Allocation-free variant of pkv_paged_attention_decode (the pages have no
+ * counterpart; it exists for callers of this library that cannot allocate
+ * device memory: an engine that gives all device memory to the KV pool and a
+ * caching allocator at start-up, a plain-C host program without a device
+ * allocator, or a latency-critical loop where cudaMalloc/cudaFree would
+ * synchronise the device).  Same arguments and result as
+ * pkv_paged_attention_decode, minus the workspace: split-K partials go to a
+ * fixed device array of PKV_STATIC_SCRATCH_BYTES (64 MiB) compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *  - The first call on a device looks the array's device address up
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - A call whose partials would need more than PKV_STATIC_SCRATCH_BYTES
+ *    (pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim,
+ *    max_context_len, partition_tokens)) returns PKV_ERR_WORKSPACE without
+ *    launching anything.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; nothing in it needs to start at zero (each partial is written
+ *    before it is read).  Calls that overlap on the GPU (other streams, other
+ *    host threads) race on the array: serialise them.
+ */
+pkv_status pkv_paged_attention_decode_static(const pkv_pool *pool, void *out,
+                                             pkv_dtype out_dtype, const void *query,
+                                             int num_seqs, int num_heads, int num_kv_heads,
+                                             const int32_t *block_tables, int max_blocks_per_seq,
+                                             const int32_t *context_lens, int max_context_len,
+                                             float scale, int partition_tokens, int flags,
+                                             void *stream);
+
 /*
  * Synchronise `stream`, read the pool's device error word into *fault_bits
  * (may be NULL) and clear it.  Returns PKV_ERR_DEVICE_FAULT if it was

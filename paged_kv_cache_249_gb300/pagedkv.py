@@ -28,7 +28,8 @@ PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 
 EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_reshape_and_cache", "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
-           "pkv_get_device_error", "pkv_status_string", "pkv_version"]
+           "pkv_get_device_error", "pkv_status_string", "pkv_version",
+           "pkv_paged_attention_decode_static"]
 
 
 class PagedKVError(RuntimeError):
@@ -68,6 +69,7 @@ def load(path: Optional[str] = None):
         "pkv_decode_workspace_bytes": (Z, [I, I, I, I, I]),
         "pkv_paged_attention_decode": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, P, Z, I, P]),
         "pkv_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
+        "pkv_paged_attention_decode_static": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, I, P]),
         "pkv_status_string": (ctypes.c_char_p, [I]),
         "pkv_version": (I, []),
     }
@@ -189,6 +191,27 @@ def paged_attention_decode(pool: BlockPool, out: torch.Tensor, query: torch.Tens
         block_tables.shape[1], context_lens.data_ptr(), int(max_context_len), float(scale),
         int(partition_tokens), _ptr(workspace), ws_bytes, int(path), _stream(stream)),
         "pkv_paged_attention_decode")
+
+
+STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def paged_attention_decode_static(pool: BlockPool, out: torch.Tensor, query: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  max_context_len: int, scale: float,
+                                  num_kv_heads: Optional[int] = None, partition_tokens: int = 0,
+                                  path: int = PATH_AUTO, stream=None) -> None:
+    """pkv_paged_attention_decode_static: the same decode with its split-K
+    partials in the library's fixed device array (no workspace argument, no
+    allocation).  For callers that cannot allocate device memory; calls that
+    overlap on the GPU share that array and race."""
+    S, H, _ = query.shape
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    _check(load().pkv_paged_attention_decode_static(
+        ctypes.byref(pool.desc), out.data_ptr(), _dtype_code(out.dtype), query.data_ptr(), S, H,
+        num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), int(max_context_len), float(scale),
+        int(partition_tokens), int(path), _stream(stream)), "pkv_paged_attention_decode_static")
 
 
 def get_device_error(pool: BlockPool, stream=None) -> int:
