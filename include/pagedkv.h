@@ -215,6 +215,12 @@ pkv_status pkv_get_device_error(const pkv_pool *pool, void *stream, uint32_t *fa
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status status);
 
+/*
+ * Description of the CUDA error behind the calling thread's most recent
+ * PKV_ERR_CUDA (static string; "no CUDA error recorded" if none).
+ */
+const char *pkv_last_cuda_error(void);
+
 /* Library ABI version (major*100 + minor). */
 int pkv_version(void);
 

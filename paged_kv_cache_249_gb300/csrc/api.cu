@@ -68,6 +68,16 @@ bool valid_geometry(int num_blocks, int block_size, int num_kv_heads, int head_d
 
 }  // namespace
 
+namespace {
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+}
+
+pkv_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PKV_OK;
+    t_last_cuda_error = e;
+    return PKV_ERR_CUDA;
+}
+
 int sm_count(int device) {
     static std::atomic<int> cache[kMaxDevices];
     if (device < 0 || device >= kMaxDevices) return 148;
@@ -85,7 +95,12 @@ using namespace pkv;
 
 extern "C" {
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 101; }
+
+const char *pkv_last_cuda_error(void) {
+    const cudaError_t e = t_last_cuda_error;
+    return e == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(e);
+}
 
 const char *pkv_status_string(pkv_status s) {
     switch (s) {
@@ -117,7 +132,7 @@ pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, i
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(dev_error, 4))
         return PKV_ERR_INVALID_ARG;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
     MapPair maps;
     std::memset(&maps, 0, sizeof(maps));
     const int rows = num_blocks * num_kv_heads * block_size;
@@ -127,10 +142,10 @@ pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, i
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (zero_fill) {
         const size_t bytes = pkv_pool_bytes(num_blocks, block_size, num_kv_heads, head_dim, dtype);
-        if (cudaMemsetAsync(k_pool, 0, bytes, st) != cudaSuccess ||
-            cudaMemsetAsync(v_pool, 0, bytes, st) != cudaSuccess)
+        if (cuda_status(cudaMemsetAsync(k_pool, 0, bytes, st)) != PKV_OK ||
+            cuda_status(cudaMemsetAsync(v_pool, 0, bytes, st)) != PKV_OK)
             return PKV_ERR_CUDA;
-        if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess)
+        if (dev_error && cuda_status(cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st)) != PKV_OK)
             return PKV_ERR_CUDA;
     }
     pool->num_blocks = num_blocks;
@@ -158,10 +173,8 @@ pkv_status pkv_block_table_upload(int32_t *dev_block_tables, const int32_t *host
     if (num_blocks > 0)
         for (size_t i = 0; i < n; ++i)
             if (host_block_tables[i] >= num_blocks) return PKV_ERR_INVALID_ARG;
-    if (cudaMemcpyAsync(dev_block_tables, host_block_tables, n * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return PKV_ERR_CUDA;
-    return PKV_OK;
+    return cuda_status(cudaMemcpyAsync(dev_block_tables, host_block_tables, n * sizeof(int32_t),
+                                       cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const void *value,
@@ -173,7 +186,7 @@ pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const vo
     if (!aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8))
         return PKV_ERR_INVALID_ARG;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
     if (dev != pool->device) return PKV_ERR_INVALID_ARG;
     return launch_reshape_and_cache(*pool, key, value, slot_mapping, num_tokens,
                                     static_cast<cudaStream_t>(stream));
@@ -235,7 +248,7 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
         mma = true;
     }
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
     if (dev != pool->device) return PKV_ERR_INVALID_ARG;
 
     const int BS = pool->block_size;
@@ -310,14 +323,15 @@ pkv_status pkv_get_device_error(const pkv_pool *pool, void *stream, uint32_t *fa
     if (fault_bits) *fault_bits = 0;
     if (!pool || pool->magic != kPoolMagic) return PKV_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (!pool->dev_error) return cudaStreamSynchronize(st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (!pool->dev_error) return cuda_status(cudaStreamSynchronize(st));
     int32_t v = 0;
-    if (cudaMemcpyAsync(&v, pool->dev_error, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (cuda_status(cudaMemcpyAsync(&v, pool->dev_error, sizeof(v), cudaMemcpyDeviceToHost, st)) !=
+            PKV_OK ||
+        cuda_status(cudaStreamSynchronize(st)) != PKV_OK)
         return PKV_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return PKV_ERR_CUDA;
     if (v != 0) {
-        if (cudaMemsetAsync(pool->dev_error, 0, sizeof(int32_t), st) != cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
+        if (cuda_status(cudaMemsetAsync(pool->dev_error, 0, sizeof(int32_t), st)) != PKV_OK ||
+            cuda_status(cudaStreamSynchronize(st)) != PKV_OK)
             return PKV_ERR_CUDA;
     }
     if (fault_bits) *fault_bits = (uint32_t)v;

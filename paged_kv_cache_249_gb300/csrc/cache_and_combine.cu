@@ -57,7 +57,7 @@ pkv_status launch_reshape_and_cache(const pkv_pool &pool, const void *key, const
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slot_mapping,
         num_tokens, pool.num_kv_heads, pool.block_size, chunks,
         (long long)pool.num_blocks * pool.block_size, pool.dev_error);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
 
 // ------------------------------------------------------------ lse_combine
@@ -110,7 +110,7 @@ pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, i
     const long long n = (long long)num_seqs * a.num_heads;
     if (n == 0) return PKV_OK;
     lse_combine_kernel<<<(unsigned)n, 128, 0, stream>>>(a, head_dim, block_size);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace pkv

@@ -58,13 +58,21 @@ struct Geom {
     static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte slabs");
 };
 
-constexpr int kDecodeWarps = 4;
+// Warps per CTA and the shared-memory budget of the staging ring (bytes per
+// CTA); compile-time tuning knobs.
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_STAGE_BUDGET
+#define PKV_STAGE_BUDGET 98304
+#endif
+constexpr int kDecodeWarps = PKV_DECODE_WARPS;
 
 template <typename T, int D, int BS>
 constexpr int decode_stages() {
     constexpr int per = kDecodeWarps * Geom<T, D, BS>::kStageBytes;
-    constexpr int n = 98304 / per;
-    return n < 1 ? 1 : (n > 6 ? 6 : n);
+    constexpr int n = PKV_STAGE_BUDGET / per;
+    return n < 1 ? 1 : (n > 8 ? 8 : n);
 }
 
 template <typename T, int D, int BS>
@@ -591,14 +599,14 @@ pkv_status launch_one(const DecodeLaunch &L) {
     static unsigned long long done_mask = 0ull;
     const unsigned long long bit = 1ull << (L.device & 63);
     if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
+        if (cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem)) != PKV_OK)
             return PKV_ERR_CUDA;
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
     }
     dim3 grid(L.num_seqs, L.args.num_kv_heads, L.args.num_parts);
     kern<<<grid, kDecodeWarps * 32, smem, L.stream>>>(*L.tmk, *L.tmv, L.args);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
 
 template <typename T, int D, int BS>

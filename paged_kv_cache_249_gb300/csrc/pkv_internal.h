@@ -63,4 +63,8 @@ pkv_status launch_reshape_and_cache(const pkv_pool &pool, const void *key, const
 
 int sm_count(int device);
 
+// Record `e` as this thread's last CUDA error (if it is one) and map it to a
+// status: PKV_OK for cudaSuccess, PKV_ERR_CUDA otherwise.
+pkv_status cuda_status(cudaError_t e);
+
 }  // namespace pkv

@@ -29,13 +29,15 @@ PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_reshape_and_cache", "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
            "pkv_get_device_error", "pkv_status_string", "pkv_version",
-           "pkv_paged_attention_decode_static"]
+           "pkv_paged_attention_decode_static", "pkv_last_cuda_error"]
 
 
 class PagedKVError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         msg = status_string(status) if _lib is not None else str(status)
+        if status == ERR_CUDA and _lib is not None:
+            msg += ": " + _lib.pkv_last_cuda_error().decode()
         super().__init__(f"{where}: {msg} (status {status})")
 
 
@@ -71,6 +73,7 @@ def load(path: Optional[str] = None):
         "pkv_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
         "pkv_paged_attention_decode_static": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, I, P]),
         "pkv_status_string": (ctypes.c_char_p, [I]),
+        "pkv_last_cuda_error": (ctypes.c_char_p, []),
         "pkv_version": (I, []),
     }
     for name, (res, args) in sig.items():
