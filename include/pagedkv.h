@@ -154,7 +154,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
  * context_lens: device int32 [num_seqs].
  * max_context_len: host upper bound on every context length (grid sizing;
  *   larger lengths are clamped and flagged PKV_FAULT_CONTEXT).
- * partition_tokens: 0 = automatic, -1 = never split, > 0 = split every
+ * partition_tokens: 0 = automatic (no split, or 512-2048-token partitions
+ *   chosen from the batch shape), -1 = never split, > 0 = split every
  *   sequence into partitions of this many tokens (a multiple of block_size,
  *   at most 8192) and combine them with a log-sum-exp pass.
  * workspace: device buffer of at least pkv_decode_workspace_bytes(...) bytes

@@ -192,18 +192,25 @@ pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const vo
                                     static_cast<cudaStream_t>(stream));
 }
 
-static int resolve_partition(int partition_tokens, int max_context_len) {
-    // 0 = automatic: partitions of kAutoPartitionTokens once a context can
-    // exceed one partition, so long and ragged contexts spread over the SMs.
-    if (partition_tokens == 0)
-        return max_context_len > kAutoPartitionTokens ? kAutoPartitionTokens : -1;
-    return partition_tokens;
+// 0 = automatic.  Partitions cost one CTA start-up each (block-table and
+// first-tile latency), so take the longest partition (2048, 1024 or 512
+// tokens) that still gives about nine waves of CTAs (three resident per SM);
+// no split when the whole context fits in one partition.  `units` is
+// num_seqs * num_kv_heads; sms <= 0 sizes for the smallest automatic choice.
+static int resolve_partition(int partition_tokens, int max_context_len, long long units, int sms) {
+    if (partition_tokens != 0) return partition_tokens;
+    if (max_context_len <= kAutoPartitionTokens) return -1;
+    if (sms <= 0) return kAutoPartitionTokens;
+    const long long target = 9ll * 3 * sms;
+    for (int pt = 2048; pt > kAutoPartitionTokens; pt /= 2)
+        if (units * ((max_context_len + pt - 1) / pt) >= target) return pt;
+    return kAutoPartitionTokens;
 }
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int partition_tokens) {
     if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
-    const int pt = resolve_partition(partition_tokens, max_context_len);
+    const int pt = resolve_partition(partition_tokens, max_context_len, 0, 0);
     if (pt <= 0) return 0;
     const size_t parts = ((size_t)max_context_len + pt - 1) / pt;
     if (parts <= 1) return 0;
@@ -272,7 +279,8 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
     a.out_bf16 = out_dtype == PKV_BF16;
     a.scale_log2 = scale * 1.4426950408889634f;
 
-    const int pt = resolve_partition(partition_tokens, ctx_cap);
+    const int pt = resolve_partition(partition_tokens, ctx_cap, (long long)num_seqs * num_kv_heads,
+                                     sm_count(dev));
     int parts = 1;
     if (pt > 0) {
         a.part_blocks = pt / BS;

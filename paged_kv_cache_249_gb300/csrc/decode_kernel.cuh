@@ -64,7 +64,7 @@ struct Geom {
 #define PKV_DECODE_WARPS 4
 #endif
 #ifndef PKV_STAGE_BUDGET
-#define PKV_STAGE_BUDGET 98304
+#define PKV_STAGE_BUDGET 65536
 #endif
 constexpr int kDecodeWarps = PKV_DECODE_WARPS;
 
@@ -75,13 +75,6 @@ constexpr int decode_stages() {
     return n < 1 ? 1 : (n > 8 ? 8 : n);
 }
 
-template <typename T, int D, int BS>
-constexpr int decode_smem_bytes() {
-    // stages + one mbarrier per stage + slack to align the base to 1024 bytes
-    return kDecodeWarps * decode_stages<T, D, BS>() * Geom<T, D, BS>::kStageBytes +
-           kDecodeWarps * decode_stages<T, D, BS>() * 8 + 1024;
-}
-
 // Per-warp state exported for the cross-warp merge: m[GP], l[GP], o[GP][D].
 template <int GP, int D>
 struct WarpState {
@@ -89,6 +82,20 @@ struct WarpState {
     float l[GP];
     float o[GP][D];
 };
+
+// Shared memory of one CTA: the staging ring, reused after the main loop for
+// the warps' exported states (whichever is larger), then one mbarrier per
+// stage, plus slack to align the base to 1024 bytes.
+template <typename T, int D, int BS, int RG>
+constexpr int decode_ring_bytes() {
+    constexpr int ring = kDecodeWarps * decode_stages<T, D, BS>() * Geom<T, D, BS>::kStageBytes;
+    constexpr int st = kDecodeWarps * (int)sizeof(WarpState<RG, D>);
+    return ring > st ? ring : st;
+}
+template <typename T, int D, int BS, int RG>
+constexpr int decode_smem_bytes() {
+    return decode_ring_bytes<T, D, BS, RG>() + kDecodeWarps * decode_stages<T, D, BS>() * 8 + 1024;
+}
 
 __device__ __forceinline__ float load_as_float(const float *p) { return *p; }
 __device__ __forceinline__ float load_as_float(const __nv_bfloat16 *p) {
@@ -273,10 +280,10 @@ struct FmaPath {
 
 // ------------------------------------------------------------ MMA compute
 
-template <int D, int BS>
+template <int D, int BS, int RG>
 struct MmaPath {
     using T = __nv_bfloat16;
-    static constexpr int GP = 16;
+    static constexpr int GP = RG;       // rows exported: 8 when the group fits rows g < 8
     static constexpr int KS = D / 16;   // k-steps of the QK^T product
     static constexpr int NT = BS / 8;   // token n-tiles per block
     static constexpr int ND = D / 8;    // head-dim n-tiles of the PV product
@@ -412,14 +419,18 @@ struct MmaPath {
             const int d = n * 8 + 2 * tig;
             st->o[gid][d] = o[n][0];
             st->o[gid][d + 1] = o[n][1];
-            st->o[gid + 8][d] = o[n][2];
-            st->o[gid + 8][d + 1] = o[n][3];
+            if constexpr (RG == 16) {
+                st->o[gid + 8][d] = o[n][2];
+                st->o[gid + 8][d + 1] = o[n][3];
+            }
         }
         if (tig == 0) {
             st->m[gid] = m0;
-            st->m[gid + 8] = m1;
             st->l[gid] = l0;
-            st->l[gid + 8] = l1;
+            if constexpr (RG == 16) {
+                st->m[gid + 8] = m1;
+                st->l[gid + 8] = l1;
+            }
         }
     }
 };
@@ -432,7 +443,7 @@ struct PathOf {
 };
 template <int D, int BS, int GP>
 struct PathOf<__nv_bfloat16, D, BS, GP, true> {
-    using type = MmaPath<D, BS>;
+    using type = MmaPath<D, BS, GP>;
 };
 
 template <typename T, int D, int BS, int GP, bool MMA>
@@ -443,8 +454,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     using Path = typename PathOf<T, D, BS, GP, MMA>::type;
     constexpr int NW = kDecodeWarps;
     constexpr int NST = decode_stages<T, D, BS>();
-    constexpr int RG = MMA ? 16 : GP;  // rows of the exported warp state
-    static_assert(sizeof(WarpState<RG, D>) <= NST * Gm::kStageBytes, "state fits in stages");
+    constexpr int RG = GP;  // rows of the exported warp state
+    constexpr int RING = decode_ring_bytes<T, D, BS, RG>();
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -453,19 +464,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const int s = blockIdx.x, g = blockIdx.y, part = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Gather this warp's first block numbers before the context length is
+    // known (bounded by the table row), so the two dependent loads overlap.
+    const int b0 = part * a.part_blocks;
+    const int tspan = min(a.max_blocks_per_seq, b0 + a.part_blocks) - b0;
+    const int nw_tbl = tspan > warp ? (tspan - warp + NW - 1) / NW : 0;
+    const int32_t *bt_row = a.block_tables + (size_t)s * a.max_blocks_per_seq;
+    auto bt_load = [&](int chunk) -> int {
+        const int i = chunk * 32 + lane;
+        return i < nw_tbl ? __ldg(bt_row + b0 + warp + i * NW) : -1;
+    };
+    int ent0 = bt_load(0), ent1 = bt_load(1);
+
     int ctx = __ldg(a.context_lens + s);
     if (ctx < 0 || ctx > a.ctx_cap) {
         if (threadIdx.x == 0 && g == 0 && part == 0) raise_fault(a.dev_error, PKV_FAULT_CONTEXT);
         ctx = ctx < 0 ? 0 : a.ctx_cap;
     }
     const int nblk = (ctx + BS - 1) / BS;
-    const int b0 = part * a.part_blocks;
     if (part > 0 && b0 >= nblk) return;  // the sequence has no such partition
     const int b1 = min(nblk, b0 + a.part_blocks);
     const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
 
     unsigned char *wstage = smem + warp * NST * Gm::kStageBytes;
-    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + NW * NST * Gm::kStageBytes) + warp * NST;
+    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + RING) + warp * NST;
     if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < NST; ++i) mbar_init(&wbar[i], 1);
@@ -475,15 +497,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
     __syncwarp();
 
-    // this warp's logical blocks: b0 + warp + i*NW, i < nw
+    // this warp's logical blocks: b0 + warp + i*NW, i < nw (nw <= nw_tbl)
     const int span = b1 - b0;
     const int nw = span > warp ? (span - warp + NW - 1) / NW : 0;
-    const int32_t *bt_row = a.block_tables + (size_t)s * a.max_blocks_per_seq;
-    auto bt_load = [&](int chunk) -> int {
-        const int i = chunk * 32 + lane;
-        return i < nw ? __ldg(bt_row + b0 + warp + i * NW) : -1;
-    };
-    int ent0 = bt_load(0), ent1 = bt_load(1);
     int cb = 0;  // chunk held in ent0
     auto bt_get = [&](int i) -> int {
         const int v0 = __shfl_sync(0xffffffffu, ent0, i & 31);
@@ -548,9 +564,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         for (int j = i; j < nw && j < i + NST; ++j) mbar_wait(&wbar[j % NST], (j / NST) & 1);
     }
 
-    // ---- merge the warps' states (each warp reuses its own stages)
-    WarpState<RG, D> *st = reinterpret_cast<WarpState<RG, D> *>(wstage);
-    path.finish(st, lane);
+    // ---- merge the warps' states in the (now idle) staging ring
+    __syncthreads();
+    WarpState<RG, D> *states = reinterpret_cast<WarpState<RG, D> *>(smem);
+    path.finish(&states[warp], lane);
     __syncthreads();
 
     const int G = a.group;
@@ -562,13 +579,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < NW; ++w)
-            M = fmaxf(M, reinterpret_cast<WarpState<RG, D> *>(smem + w * NST * Gm::kStageBytes)->m[r]);
+            M = fmaxf(M, states[w].m[r]);
         float L = 0.f, O = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const WarpState<RG, D> *ws =
-                    reinterpret_cast<const WarpState<RG, D> *>(smem + w * NST * Gm::kStageBytes);
+                const WarpState<RG, D> *ws = &states[w];
                 const float f = fast_exp2(ws->m[r] - M);
                 L += ws->l[r] * f;
                 O += ws->o[r][d] * f;
@@ -593,7 +609,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 template <typename T, int D, int BS, int GP, bool MMA>
 pkv_status launch_one(const DecodeLaunch &L) {
     auto kern = paged_decode_kernel<T, D, BS, GP, MMA>;
-    constexpr int smem = decode_smem_bytes<T, D, BS>();
+    constexpr int smem = decode_smem_bytes<T, D, BS, GP>();
     static_assert(smem <= 227 * 1024, "shared memory budget");
     // Raise the dynamic shared-memory limit once per device for this kernel.
     static unsigned long long done_mask = 0ull;
@@ -612,7 +628,9 @@ pkv_status launch_one(const DecodeLaunch &L) {
 template <typename T, int D, int BS>
 pkv_status launch_bs(const DecodeLaunch &L) {
     if constexpr (sizeof(T) == 2) {
-        if (L.mma) return launch_one<T, D, BS, 16, true>(L);
+        if (L.mma)
+            return L.group_pad <= 8 ? launch_one<T, D, BS, 8, true>(L)
+                                    : launch_one<T, D, BS, 16, true>(L);
     }
     switch (L.group_pad) {
         case 1: return launch_one<T, D, BS, 1, false>(L);
