@@ -24,6 +24,7 @@ import sys
 import threading
 import time
 
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

@@ -49,7 +49,8 @@ typedef enum {
     PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, block_size, group, dtype */
     PKV_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
     PKV_ERR_WORKSPACE = 4,     /* split-K workspace missing or too small */
-    PKV_ERR_DEVICE_FAULT = 5   /* the device error word was non-zero */
+    PKV_ERR_DEVICE_FAULT = 5,  /* the device error word was non-zero */
+    PKV_ERR_OUT_OF_BLOCKS = 6  /* the block manager has no free block left */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -205,6 +206,59 @@ pkv_status pkv_paged_attention_decode_static(const pkv_pool *pool, void *out,
                                              const int32_t *context_lens, int max_context_len,
                                              float scale, int partition_tokens, int flags,
                                              void *stream);
+
+/*
+ * Copy whole physical blocks (every kv head, K and V): block dst[i] becomes a
+ * copy of block src[i], i < num_pairs.  src/dst: device int32 arrays.  Used
+ * for the block manager's copy-on-write, before the new token is written.
+ * A pair naming a block outside the pool sets PKV_FAULT_BLOCK_ID and is
+ * skipped.  Pairs of one call must not chain (no dst is another pair's src).
+ */
+pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *src, const int32_t *dst,
+                           int num_pairs, void *stream);
+
+/*
+ * Host-side block manager (host memory only, no CUDA call, not thread-safe).
+ * It hands out physical blocks of a pool of num_blocks blocks as sequences
+ * grow and takes them back when they finish (Qualiteg, "1-3 ... add or
+ * remove blocks as needed"), keeps each sequence's logical-to-physical block
+ * list ("There are logical blocks and physical blocks ..."), and lets forked
+ * sequences share blocks (prompt-prefix sharing) with reference counts:
+ * appending to a shared, partly filled last block first moves the writer to
+ * a fresh block and queues a (src, dst) copy for pkv_copy_blocks.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* New manager over blocks 0..num_blocks-1, all free; lowest ids first. */
+pkv_status pkv_bm_create(int num_blocks, int block_size, pkv_block_manager **out);
+void pkv_bm_destroy(pkv_block_manager *bm);
+/* Free blocks, or -1 for a NULL manager. */
+int pkv_bm_free_blocks(const pkv_block_manager *bm);
+/* Reference count of a physical block (0 = free), -1 if out of range. */
+int pkv_bm_refcount(const pkv_block_manager *bm, int32_t block);
+/* Register a new sequence of num_tokens tokens (its prompt) and allocate its
+ * blocks; slots (may be NULL) receives each token's flat pool slot, for the
+ * cache write.  PKV_ERR_OUT_OF_BLOCKS leaves the manager unchanged. */
+pkv_status pkv_bm_add_sequence(pkv_block_manager *bm, int64_t seq_id, int64_t num_tokens,
+                               int64_t *slots);
+/* child shares every block of parent (reference counts + 1). */
+pkv_status pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t child);
+/* Grow a sequence by one token; *slot receives the new token's pool slot.
+ * May allocate a block, or copy-on-write a shared last block. */
+pkv_status pkv_bm_append_token(pkv_block_manager *bm, int64_t seq_id, int64_t *slot);
+/* Drop a sequence; blocks no other sequence holds become free. */
+pkv_status pkv_bm_free_sequence(pkv_block_manager *bm, int64_t seq_id);
+/* Tokens of a sequence, -1 if unknown. */
+int64_t pkv_bm_context_len(const pkv_block_manager *bm, int64_t seq_id);
+/* Pending copy-on-write copies, and draining them (returns how many were
+ * written to src/dst, at most capacity). */
+int pkv_bm_pending_copies(const pkv_block_manager *bm);
+int pkv_bm_take_copies(pkv_block_manager *bm, int32_t *src, int32_t *dst, int capacity);
+/* Host block tables [num_seqs][max_blocks_per_seq] (-1 padded) and context
+ * lengths of the listed sequences, ready for pkv_block_table_upload. */
+pkv_status pkv_bm_block_tables(const pkv_block_manager *bm, const int64_t *seq_ids, int num_seqs,
+                               int max_blocks_per_seq, int32_t *block_tables,
+                               int32_t *context_lens);
 
 /*
  * Synchronise `stream`, read the pool's device error word into *fault_bits

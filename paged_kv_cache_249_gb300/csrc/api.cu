@@ -110,6 +110,7 @@ const char *pkv_status_string(pkv_status s) {
         case PKV_ERR_CUDA: return "CUDA error";
         case PKV_ERR_WORKSPACE: return "workspace missing or too small";
         case PKV_ERR_DEVICE_FAULT: return "device reported a data fault";
+        case PKV_ERR_OUT_OF_BLOCKS: return "no free block in the pool";
     }
     return "unknown status";
 }
@@ -325,6 +326,17 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
         st = pool->head_dim == 64 ? launch_decode_f32_d64(L) : launch_decode_f32_d128(L);
     if (st != PKV_OK || parts <= 1) return st;
     return launch_lse_combine(a, num_seqs, pool->head_dim, BS, L.stream);
+}
+
+pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *src, const int32_t *dst,
+                           int num_pairs, void *stream) {
+    if (!pool || pool->magic != kPoolMagic || num_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!src || !dst || !aligned(src, 4) || !aligned(dst, 4)) return PKV_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
+    if (dev != pool->device) return PKV_ERR_INVALID_ARG;
+    return launch_copy_blocks(*pool, src, dst, num_pairs, static_cast<cudaStream_t>(stream));
 }
 
 pkv_status pkv_get_device_error(const pkv_pool *pool, void *stream, uint32_t *fault_bits) {

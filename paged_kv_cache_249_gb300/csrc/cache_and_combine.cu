@@ -60,6 +60,44 @@ pkv_status launch_reshape_and_cache(const pkv_pool &pool, const void *key, const
     return cuda_status(cudaGetLastError());
 }
 
+// ------------------------------------------------------------ copy_blocks
+//
+// Copy-on-write of shared blocks: whole physical blocks (all kv heads) of K
+// and V, one 16-byte chunk per thread.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
+                       const int32_t *__restrict__ src, const int32_t *__restrict__ dst,
+                       int num_pairs, long long chunks_per_block, int num_blocks,
+                       int32_t *dev_error) {
+    const long long total = chunks_per_block * num_pairs;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int p = (int)(idx / chunks_per_block);
+        const long long c = idx - (long long)p * chunks_per_block;
+        const int s = __ldg(src + p), d = __ldg(dst + p);
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+            if (c == 0) raise_fault(dev_error, PKV_FAULT_BLOCK_ID);
+            continue;
+        }
+        k_pool[(size_t)d * chunks_per_block + c] = k_pool[(size_t)s * chunks_per_block + c];
+        v_pool[(size_t)d * chunks_per_block + c] = v_pool[(size_t)s * chunks_per_block + c];
+    }
+}
+
+pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const int32_t *dst,
+                              int num_pairs, cudaStream_t stream) {
+    const int elem = pool.dtype == PKV_BF16 ? 2 : 4;
+    const long long chunks =
+        (long long)pool.num_kv_heads * pool.block_size * pool.head_dim * elem / 16;
+    long long blocks = (chunks * num_pairs + 255) / 256;
+    const long long cap = (long long)sm_count(pool.device) * 8;
+    if (blocks > cap) blocks = cap;
+    copy_blocks_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<uint4 *>(pool.k_pool), static_cast<uint4 *>(pool.v_pool), src, dst, num_pairs,
+        chunks, pool.num_blocks, pool.dev_error);
+    return cuda_status(cudaGetLastError());
+}
+
 // ------------------------------------------------------------ lse_combine
 //
 // A context split into partitions p = 0..P-1 has, per query head, normalised

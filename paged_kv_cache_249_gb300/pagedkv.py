@@ -18,7 +18,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 # pkv_status
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_FAULT = range(6)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_FAULT,
+ ERR_OUT_OF_BLOCKS) = range(7)
 # pkv_dtype
 F32, BF16 = 0, 1
 # device fault bits
@@ -29,7 +30,11 @@ PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_reshape_and_cache", "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
            "pkv_get_device_error", "pkv_status_string", "pkv_version",
-           "pkv_paged_attention_decode_static", "pkv_last_cuda_error"]
+           "pkv_paged_attention_decode_static", "pkv_last_cuda_error", "pkv_copy_blocks",
+           "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_free_blocks", "pkv_bm_refcount",
+           "pkv_bm_add_sequence", "pkv_bm_fork", "pkv_bm_append_token", "pkv_bm_free_sequence",
+           "pkv_bm_context_len", "pkv_bm_pending_copies", "pkv_bm_take_copies",
+           "pkv_bm_block_tables"]
 
 
 class PagedKVError(RuntimeError):
@@ -62,6 +67,7 @@ def load(path: Optional[str] = None):
         raise ImportError(f"{p} is missing: build it with paged_kv_cache_249_gb300.build.build()")
     lib = ctypes.CDLL(p)
     I, P, Z, F = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+    L = ctypes.c_int64
     PP = ctypes.POINTER(pkv_pool)
     sig = {
         "pkv_pool_bytes": (Z, [I, I, I, I, I]),
@@ -72,6 +78,19 @@ def load(path: Optional[str] = None):
         "pkv_paged_attention_decode": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, P, Z, I, P]),
         "pkv_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
         "pkv_paged_attention_decode_static": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, I, P]),
+        "pkv_copy_blocks": (I, [PP, P, P, I, P]),
+        "pkv_bm_create": (I, [I, I, ctypes.POINTER(P)]),
+        "pkv_bm_destroy": (None, [P]),
+        "pkv_bm_free_blocks": (I, [P]),
+        "pkv_bm_refcount": (I, [P, ctypes.c_int32]),
+        "pkv_bm_add_sequence": (I, [P, L, L, P]),
+        "pkv_bm_fork": (I, [P, L, L]),
+        "pkv_bm_append_token": (I, [P, L, ctypes.POINTER(L)]),
+        "pkv_bm_free_sequence": (I, [P, L]),
+        "pkv_bm_context_len": (L, [P, L]),
+        "pkv_bm_pending_copies": (I, [P]),
+        "pkv_bm_take_copies": (I, [P, P, P, I]),
+        "pkv_bm_block_tables": (I, [P, P, I, I, P, P]),
         "pkv_status_string": (ctypes.c_char_p, [I]),
         "pkv_last_cuda_error": (ctypes.c_char_p, []),
         "pkv_version": (I, []),
@@ -215,6 +234,73 @@ def paged_attention_decode_static(pool: BlockPool, out: torch.Tensor, query: tor
         num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, block_tables.data_ptr(),
         block_tables.shape[1], context_lens.data_ptr(), int(max_context_len), float(scale),
         int(partition_tokens), int(path), _stream(stream)), "pkv_paged_attention_decode_static")
+
+
+def copy_blocks(pool: BlockPool, src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """Device copy of whole blocks src[i] -> dst[i] (int32 device tensors)."""
+    assert src.dtype == torch.int32 and dst.dtype == torch.int32 and src.numel() == dst.numel()
+    _check(load().pkv_copy_blocks(ctypes.byref(pool.desc), src.data_ptr(), dst.data_ptr(),
+                                  src.numel(), _stream(stream)), "pkv_copy_blocks")
+
+
+class BlockManager:
+    """Host block manager of a pool (C++ behind the C ABI; host memory only)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self.lib = load()
+        self.block_size = block_size
+        h = ctypes.c_void_p()
+        _check(self.lib.pkv_bm_create(num_blocks, block_size, ctypes.byref(h)), "pkv_bm_create")
+        self.h = h
+
+    def __del__(self):
+        if getattr(self, "h", None) and self.h.value:
+            self.lib.pkv_bm_destroy(self.h)
+            self.h = None
+
+    @property
+    def free_blocks(self) -> int:
+        return self.lib.pkv_bm_free_blocks(self.h)
+
+    def refcount(self, block: int) -> int:
+        return self.lib.pkv_bm_refcount(self.h, block)
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> np.ndarray:
+        slots = np.empty(max(num_tokens, 1), dtype=np.int64)
+        _check(self.lib.pkv_bm_add_sequence(self.h, seq_id, num_tokens, slots.ctypes.data),
+               "pkv_bm_add_sequence")
+        return slots[:num_tokens]
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(self.lib.pkv_bm_fork(self.h, parent, child), "pkv_bm_fork")
+
+    def append_token(self, seq_id: int) -> int:
+        slot = ctypes.c_int64(-1)
+        _check(self.lib.pkv_bm_append_token(self.h, seq_id, ctypes.byref(slot)),
+               "pkv_bm_append_token")
+        return slot.value
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check(self.lib.pkv_bm_free_sequence(self.h, seq_id), "pkv_bm_free_sequence")
+
+    def context_len(self, seq_id: int) -> int:
+        return self.lib.pkv_bm_context_len(self.h, seq_id)
+
+    def take_copies(self):
+        n = self.lib.pkv_bm_pending_copies(self.h)
+        src = np.empty(max(n, 1), dtype=np.int32)
+        dst = np.empty(max(n, 1), dtype=np.int32)
+        got = self.lib.pkv_bm_take_copies(self.h, src.ctypes.data, dst.ctypes.data, n)
+        return src[:got], dst[:got]
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        bt = np.empty((ids.size, max_blocks_per_seq), dtype=np.int32)
+        cl = np.empty(ids.size, dtype=np.int32)
+        _check(self.lib.pkv_bm_block_tables(self.h, ids.ctypes.data, ids.size, max_blocks_per_seq,
+                                            bt.ctypes.data, cl.ctypes.data),
+               "pkv_bm_block_tables")
+        return bt, cl
 
 
 def get_device_error(pool: BlockPool, stream=None) -> int:
