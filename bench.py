@@ -303,6 +303,35 @@ def run_native(args, world: int, rank: int) -> dict | None:
     value = whole_job_rate(ab["kv_logical"] * args.steps, world, max_s) / 1e9
     seqs_per_s = whole_job_rate(w.num_seqs * args.steps, world, max_s)
 
+    # ---- the same decode over a contiguous cache (what paging costs)
+    paging = None
+    if world == 1 and not args.no_contiguous:
+        cache = pagedkv.ContiguousCache.from_paged(w, k_pool=dw.k_pool, v_pool=dw.v_pool)
+        cout = torch.empty_like(dw.out)
+
+        def contig_decode():
+            pagedkv.contiguous_attention_decode(cache, cout, dw.q, dw.context_lens,
+                                                dw.max_context_len, w.scale,
+                                                partition_tokens=dw.partition_tokens,
+                                                workspace=dw.workspace)
+        for _ in range(args.warmup):
+            contig_decode()
+        torch.cuda.synchronize()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a_, b_ in cev:
+            a_.record(stream)
+            contig_decode()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        c_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in cev])) * 1e3
+        p_us = float(np.mean(dec_ms)) * 1e3
+        paging = {"paged_decode_us": round(p_us, 2), "contiguous_decode_us": round(c_us, 2),
+                  "paged_over_contiguous": round(p_us / c_us, 4),
+                  "same_output": bool(torch.equal(cout.view(torch.int16), dw.out.view(torch.int16)))}
+        del cache, cout
+        torch.cuda.empty_cache()
+
     # ---- end to end through the C ABI with host buffers
     pin = lambda t: t.pin_memory()  # noqa: E731
     q_h, nk_h, nv_h = pin(w.q), pin(w.new_key), pin(w.new_value)
@@ -365,6 +394,7 @@ def run_native(args, world: int, rank: int) -> dict | None:
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3 / args.steps, 5)},
         "gpu_launches": launches_per_step * args.steps,
+        "paging_overhead": paging,
         "clocks": clock_info,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -418,6 +448,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-contiguous", action="store_true",
+                   help="skip the contiguous-cache comparison")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--reference-seconds", type=float, default=120.0,

@@ -83,6 +83,8 @@ typedef struct pkv_pool {
     int head_dim;
     pkv_dtype dtype;
     int device;
+    int layout;                   /* 0 = paged block pool, 1 = contiguous per-sequence cache */
+    int num_seqs;                 /* contiguous layout only: sequences the cache holds */
     void *k_pool;
     void *v_pool;
     int32_t *dev_error;           /* device int32 or NULL */
@@ -206,6 +208,29 @@ pkv_status pkv_paged_attention_decode_static(const pkv_pool *pool, void *out,
                                              const int32_t *context_lens, int max_context_len,
                                              float scale, int partition_tokens, int flags,
                                              void *stream);
+
+/*
+ * Contiguous-layout variant, for measuring what paging costs (the pages note
+ * that a paged kernel is slower than one reading contiguous K and V: the
+ * Hacker News thread, and vAttention section 3.1).  Not part of the paged
+ * path: it reads a conventional cache where sequence s, kv head g holds its
+ * tokens in rows [s][g][0 .. capacity) of a [num_seqs][num_kv_heads]
+ * [capacity][head_dim] K (and V) buffer.  capacity: a multiple of 16.  The
+ * kernel is the paged kernel with the block table replaced by identity
+ * numbering, so for the same tokens it returns bitwise the paged result.
+ */
+pkv_status pkv_contiguous_cache_init(pkv_pool *cache, int num_seqs, int capacity,
+                                     int num_kv_heads, int head_dim, pkv_dtype dtype,
+                                     void *k_cache, void *v_cache, int32_t *dev_error,
+                                     int zero_fill, void *stream);
+/* Decode attention over a contiguous cache; arguments as
+ * pkv_paged_attention_decode without the block table. */
+pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv_dtype out_dtype,
+                                           const void *query, int num_seqs, int num_heads,
+                                           int num_kv_heads, const int32_t *context_lens,
+                                           int max_context_len, float scale,
+                                           int partition_tokens, void *workspace,
+                                           size_t workspace_bytes, int flags, void *stream);
 
 /*
  * Copy whole physical blocks (every kv head, K and V): block dst[i] becomes a

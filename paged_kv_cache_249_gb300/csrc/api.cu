@@ -155,6 +155,8 @@ pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, i
     pool->head_dim = head_dim;
     pool->dtype = dtype;
     pool->device = dev;
+    pool->layout = 0;
+    pool->num_seqs = 0;
     pool->k_pool = k_pool;
     pool->v_pool = v_pool;
     pool->dev_error = dev_error;
@@ -180,7 +182,7 @@ pkv_status pkv_block_table_upload(int32_t *dev_block_tables, const int32_t *host
 
 pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const void *value,
                                  const int64_t *slot_mapping, int num_tokens, void *stream) {
-    if (!pool || pool->magic != kPoolMagic) return PKV_ERR_INVALID_ARG;
+    if (!pool || pool->magic != kPoolMagic || pool->layout != 0) return PKV_ERR_INVALID_ARG;
     if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0) return PKV_OK;
     if (!key || !value || !slot_mapping) return PKV_ERR_INVALID_ARG;
@@ -219,14 +221,15 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
     return round_up(rows * head_dim * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
 }
 
-pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype out_dtype,
-                                      const void *query, int num_seqs, int num_heads,
-                                      int num_kv_heads, const int32_t *block_tables,
-                                      int max_blocks_per_seq, const int32_t *context_lens,
-                                      int max_context_len, float scale, int partition_tokens,
-                                      void *workspace, size_t workspace_bytes, int flags,
-                                      void *stream) {
-    if (!pool || pool->magic != kPoolMagic) return PKV_ERR_INVALID_ARG;
+static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_dtype out_dtype,
+                              const void *query, int num_seqs, int num_heads, int num_kv_heads,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int max_context_len, float scale,
+                              int partition_tokens, void *workspace, size_t workspace_bytes,
+                              int flags, void *stream) {
+    if (!pool || pool->magic != kPoolMagic || pool->layout != (contig ? 1 : 0))
+        return PKV_ERR_INVALID_ARG;
+    if (contig && num_seqs > pool->num_seqs) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
         max_context_len < 0)
         return PKV_ERR_INVALID_ARG;
@@ -241,7 +244,7 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
         (partition_tokens > 0 && partition_tokens % pool->block_size != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !query || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+    if (!out || !query || (!block_tables && !contig) || !context_lens) return PKV_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(query, 16) || !aligned(block_tables, 4) ||
         !aligned(context_lens, 4))
         return PKV_ERR_INVALID_ARG;
@@ -278,6 +281,7 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
     a.num_blocks = pool->num_blocks;
     a.ctx_cap = ctx_cap;
     a.out_bf16 = out_dtype == PKV_BF16;
+    a.contig = contig ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
 
     const int pt = resolve_partition(partition_tokens, ctx_cap, (long long)num_seqs * num_kv_heads,
@@ -328,9 +332,53 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
     return launch_lse_combine(a, num_seqs, pool->head_dim, BS, L.stream);
 }
 
+pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype out_dtype,
+                                      const void *query, int num_seqs, int num_heads,
+                                      int num_kv_heads, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *context_lens,
+                                      int max_context_len, float scale, int partition_tokens,
+                                      void *workspace, size_t workspace_bytes, int flags,
+                                      void *stream) {
+    return decode_impl(pool, false, out, out_dtype, query, num_seqs, num_heads, num_kv_heads,
+                       block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                       partition_tokens, workspace, workspace_bytes, flags, stream);
+}
+
+pkv_status pkv_contiguous_cache_init(pkv_pool *cache, int num_seqs, int capacity,
+                                     int num_kv_heads, int head_dim, pkv_dtype dtype,
+                                     void *k_cache, void *v_cache, int32_t *dev_error,
+                                     int zero_fill, void *stream) {
+    const int BS = 16;
+    if (!cache || num_seqs <= 0 || capacity <= 0 || capacity % BS != 0) return PKV_ERR_INVALID_ARG;
+    const long long rows = (long long)num_seqs * num_kv_heads * capacity;
+    if (rows >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+    // the same descriptor as a pool whose "blocks" are the runs of 16 rows
+    const pkv_status st = pkv_block_pool_init(cache, (int)(rows / ((long long)num_kv_heads * BS)),
+                                              BS, num_kv_heads, head_dim, dtype, k_cache, v_cache,
+                                              dev_error, zero_fill, stream);
+    if (st != PKV_OK) return st;
+    cache->layout = 1;
+    cache->num_seqs = num_seqs;
+    cache->num_blocks = capacity / BS;  // blocks per (sequence, kv head) run
+    return PKV_OK;
+}
+
+pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv_dtype out_dtype,
+                                           const void *query, int num_seqs, int num_heads,
+                                           int num_kv_heads, const int32_t *context_lens,
+                                           int max_context_len, float scale,
+                                           int partition_tokens, void *workspace,
+                                           size_t workspace_bytes, int flags, void *stream) {
+    if (!cache) return PKV_ERR_INVALID_ARG;
+    return decode_impl(cache, true, out, out_dtype, query, num_seqs, num_heads, num_kv_heads,
+                       nullptr, cache->num_blocks, context_lens, max_context_len, scale,
+                       partition_tokens, workspace, workspace_bytes, flags, stream);
+}
+
 pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *src, const int32_t *dst,
                            int num_pairs, void *stream) {
-    if (!pool || pool->magic != kPoolMagic || num_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (!pool || pool->magic != kPoolMagic || pool->layout != 0 || num_pairs < 0)
+        return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
     if (!src || !dst || !aligned(src, 4) || !aligned(dst, 4)) return PKV_ERR_INVALID_ARG;
     int dev = 0;

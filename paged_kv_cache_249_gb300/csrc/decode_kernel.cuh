@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const int32_t *bt_row = a.block_tables + (size_t)s * a.max_blocks_per_seq;
     auto bt_load = [&](int chunk) -> int {
         const int i = chunk * 32 + lane;
-        return i < nw_tbl ? __ldg(bt_row + b0 + warp + i * NW) : -1;
+        if (i >= nw_tbl) return -1;
+        return a.contig ? b0 + warp + i * NW : __ldg(bt_row + b0 + warp + i * NW);
     };
     int ent0 = bt_load(0), ent1 = bt_load(1);
 
@@ -513,7 +514,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                 mbar_arrive_expect_tx(bar, Gm::kStageBytes);
                 unsigned char *dk = wstage + (i % NST) * Gm::kStageBytes;
                 unsigned char *dv = dk + Gm::kTileBytes;
-                const int y = (pb * a.num_kv_heads + g) * BS;
+                const int y = a.contig ? ((s * a.num_kv_heads + g) * a.num_blocks + pb) * BS
+                                       : (pb * a.num_kv_heads + g) * BS;
 #pragma unroll
                 for (int sl = 0; sl < Gm::kSlabs; ++sl) {
                     tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);

@@ -33,6 +33,7 @@ struct DecodeArgs {
     int part_blocks;            // KV blocks per partition (one CTA each)
     int num_parts;              // gridDim.z: partitions of the longest allowed context
     int out_bf16;
+    int contig;                 // 1: contiguous cache, block b of (s, g) is row run (s*Hkv+g)*num_blocks+b
     float scale_log2;           // scale * log2(e)
 };
 

@@ -34,7 +34,8 @@ EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_free_blocks", "pkv_bm_refcount",
            "pkv_bm_add_sequence", "pkv_bm_fork", "pkv_bm_append_token", "pkv_bm_free_sequence",
            "pkv_bm_context_len", "pkv_bm_pending_copies", "pkv_bm_take_copies",
-           "pkv_bm_block_tables"]
+           "pkv_bm_block_tables", "pkv_contiguous_cache_init",
+           "pkv_contiguous_attention_decode"]
 
 
 class PagedKVError(RuntimeError):
@@ -50,7 +51,7 @@ class pkv_pool(ctypes.Structure):
     _fields_ = [("magic", ctypes.c_uint32), ("num_blocks", ctypes.c_int),
                 ("block_size", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("device", ctypes.c_int),
-                ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("layout", ctypes.c_int), ("num_seqs", ctypes.c_int), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
                 ("dev_error", ctypes.c_void_p), ("tma", ctypes.c_uint64 * 32)]
 
 
@@ -79,6 +80,8 @@ def load(path: Optional[str] = None):
         "pkv_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
         "pkv_paged_attention_decode_static": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, I, P]),
         "pkv_copy_blocks": (I, [PP, P, P, I, P]),
+        "pkv_contiguous_cache_init": (I, [PP, I, I, I, I, I, P, P, P, I, P]),
+        "pkv_contiguous_attention_decode": (I, [PP, P, I, P, I, I, I, P, I, F, I, P, Z, I, P]),
         "pkv_bm_create": (I, [I, I, ctypes.POINTER(P)]),
         "pkv_bm_destroy": (None, [P]),
         "pkv_bm_free_blocks": (I, [P]),
@@ -234,6 +237,60 @@ def paged_attention_decode_static(pool: BlockPool, out: torch.Tensor, query: tor
         num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, block_tables.data_ptr(),
         block_tables.shape[1], context_lens.data_ptr(), int(max_context_len), float(scale),
         int(partition_tokens), int(path), _stream(stream)), "pkv_paged_attention_decode_static")
+
+
+class ContiguousCache:
+    """A conventional [S][Hkv][capacity][D] K/V cache (the layout a paged
+    pool replaces), described to the library for the paging-overhead
+    comparison."""
+
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 dev_error: Optional[torch.Tensor] = None, stream=None):
+        assert k_cache.shape == v_cache.shape and k_cache.is_contiguous() and v_cache.is_contiguous()
+        S, Hkv, cap, D = k_cache.shape
+        self.k_cache, self.v_cache, self.dev_error = k_cache, v_cache, dev_error
+        self.desc = pkv_pool()
+        _check(load().pkv_contiguous_cache_init(ctypes.byref(self.desc), S, cap, Hkv, D,
+                                                _dtype_code(k_cache.dtype), k_cache.data_ptr(),
+                                                v_cache.data_ptr(), _ptr(dev_error), 0,
+                                                _stream(stream)), "pkv_contiguous_cache_init")
+        self.num_kv_heads = Hkv
+
+    @staticmethod
+    def from_paged(w, capacity: Optional[int] = None, device="cuda", k_pool=None,
+                   v_pool=None) -> "ContiguousCache":
+        """Gather a paged Workload's tokens (logical order) into a contiguous
+        cache, from its host pools or from the given (device) pools."""
+        BS = w.block_size
+        cap = capacity or max(BS, -(-w.max_context_len // BS) * BS)
+        S, Hkv, D = w.num_seqs, w.num_kv_heads, w.head_dim
+        k = torch.zeros(S, Hkv, cap, D, dtype=w.torch_dtype, device=device)
+        v = torch.zeros_like(k)
+        kp = (k_pool if k_pool is not None else w.k_pool).to(device)
+        vp = (v_pool if v_pool is not None else w.v_pool).to(device)
+        for s in range(S):
+            n = int(w.context_lens[s])
+            nb = -(-n // BS)
+            if nb == 0:
+                continue
+            blocks = torch.from_numpy(w.block_tables[s, :nb].astype(np.int64)).to(device)
+            # [nb][Hkv][BS][D] -> [Hkv][nb*BS][D]
+            k[s, :, :nb * BS] = kp[blocks].permute(1, 0, 2, 3).reshape(Hkv, nb * BS, D)
+            v[s, :, :nb * BS] = vp[blocks].permute(1, 0, 2, 3).reshape(Hkv, nb * BS, D)
+        return ContiguousCache(k, v)
+
+
+def contiguous_attention_decode(cache: ContiguousCache, out: torch.Tensor, query: torch.Tensor,
+                                context_lens: torch.Tensor, max_context_len: int, scale: float,
+                                partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                                path: int = PATH_AUTO, stream=None) -> None:
+    S, H, _ = query.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_contiguous_attention_decode(
+        ctypes.byref(cache.desc), out.data_ptr(), _dtype_code(out.dtype), query.data_ptr(), S, H,
+        cache.num_kv_heads, context_lens.data_ptr(), int(max_context_len), float(scale),
+        int(partition_tokens), _ptr(workspace), ws_bytes, int(path), _stream(stream)),
+        "pkv_contiguous_attention_decode")
 
 
 def copy_blocks(pool: BlockPool, src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
