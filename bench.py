@@ -40,7 +40,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per decode launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by workload, valid only while the kernel
 # sources hash to `src`.  Filled in from the profiles summaries.
-NCU_TRAFFIC: dict = {}
+NCU_TRAFFIC: dict = {
+    # profiles/paged_decode_kernel_mha_7b_gqa_8b.md
+    "mha_7b": {"bytes": 1105897000 + 5756160, "src": "5ef0ae93b6c54d39"},
+    "gqa_8b": {"bytes": 2374157000 + 13745152, "src": "5ef0ae93b6c54d39"},
+}
 
 
 def kernel_source_hash() -> str:
