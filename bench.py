@@ -42,18 +42,27 @@ FALLBACK_HBM_GBS = 6800.0
 # sources hash to `src`.  Filled in from the profiles summaries.
 NCU_TRAFFIC: dict = {
     # profiles/paged_decode_kernel_mha_7b_gqa_8b.md
-    "mha_7b": {"bytes": 1105897000 + 5756160, "src": "5ef0ae93b6c54d39"},
-    "gqa_8b": {"bytes": 2374157000 + 13745152, "src": "5ef0ae93b6c54d39"},
+    ("mha_7b", "plain"): {"bytes": 1105897000 + 5756160, "src": "2c19345f8540f6ba"},
+    ("gqa_8b", "plain"): {"bytes": 2374157000 + 13745152, "src": "2c19345f8540f6ba"},
 }
 
 
-def kernel_source_hash() -> str:
+# Source files of each timed kernel family (a change to any of them makes the
+# recorded DRAM traffic stale).
+KERNEL_SOURCES = {
+    "plain": ["decode_kernel.cuh", "pkv_device.cuh", "decode_bf16_d128.cu", "decode_bf16_d64.cu",
+              "decode_f32_d128.cu", "decode_f32_d64.cu", "cache_and_combine.cu"],
+    "shared": ["shared_prefix_kernel.cuh", "shared_prefix.cu", "shared_prefix_d128.cu",
+               "decode_kernel.cuh", "pkv_device.cuh"],
+}
+
+
+def kernel_source_hash(family: str = "plain") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_249_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in sorted(KERNEL_SOURCES[family]):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -268,12 +277,24 @@ def run_native(args, world: int, rank: int) -> dict | None:
     # the untouched pools for the CPU baseline
     dw = pagedkv.DeviceWorkload(w, out_dtype=torch.bfloat16)
     split = dw.workspace is not None
-    launches_per_step = 2 + (1 if split else 0)
+    shared = args.decode == "shared" or (args.decode == "auto" and w.group_size > 1)
+    if shared:
+        dw.shared_prefix_setup()
+        decode = dw.decode_shared_prefix
+        launches_per_step = 1 + 3  # cache write, plan, decode, combine
+    else:
+        decode = dw.decode
+        launches_per_step = 2 + (1 if split else 0)
+    family = "shared" if shared else "plain"
     stream = torch.cuda.current_stream()
     ab = algorithmic_bytes(w)
 
+    def step():
+        pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+        decode()
+
     for _ in range(args.warmup):
-        dw.step()
+        step()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -288,7 +309,7 @@ def run_native(args, world: int, rank: int) -> dict | None:
     for k in range(args.steps):
         pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
         ev_dec[k][0].record(stream)
-        dw.decode()
+        decode()
         ev_dec[k][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -307,9 +328,31 @@ def run_native(args, world: int, rank: int) -> dict | None:
     value = whole_job_rate(ab["kv_logical"] * args.steps, world, max_s) / 1e9
     seqs_per_s = whole_job_rate(w.num_seqs * args.steps, world, max_s)
 
+    # ---- the plain decode kernel on the same batch (what prefix awareness buys)
+    plain_cmp = None
+    if shared and world == 1:
+        ref_out = dw.out.clone()
+        for _ in range(args.warmup):
+            dw.decode()
+        torch.cuda.synchronize()
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a_, b_ in pev:
+            a_.record(stream)
+            dw.decode()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        pl_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in pev])) * 1e3
+        sp_us = float(np.mean(dec_ms)) * 1e3
+        plain_cmp = {"shared_prefix_decode_us": round(sp_us, 2), "plain_decode_us": round(pl_us, 2),
+                     "plain_over_shared": round(pl_us / sp_us, 4),
+                     "max_abs_diff": float((dw.out.float() - ref_out.float()).abs().max())}
+        decode()  # leave the shared-prefix output in dw.out
+        torch.cuda.synchronize()
+
     # ---- the same decode over a contiguous cache (what paging costs)
     paging = None
-    if world == 1 and not args.no_contiguous:
+    if world == 1 and not args.no_contiguous and not shared:
         cache = pagedkv.ContiguousCache.from_paged(w, k_pool=dw.k_pool, v_pool=dw.v_pool)
         cout = torch.empty_like(dw.out)
 
@@ -353,7 +396,7 @@ def run_native(args, world: int, rank: int) -> dict | None:
         dw.slot_mapping.copy_(sm_h, non_blocking=True)
         dw.context_lens.copy_(cl_h, non_blocking=True)
         pagedkv.block_table_upload(dw.block_tables, bt_h, w.num_blocks)
-        dw.step()
+        step()
         out_h.copy_(dw.out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -376,8 +419,8 @@ def run_native(args, world: int, rank: int) -> dict | None:
     dec_avg_s = float(np.mean(dec_ms)) / 1e3
     achieved = ab["decode_launch"] / dec_avg_s / 1e9
     traffic = None
-    rec = NCU_TRAFFIC.get(args.workload)
-    if rec and rec.get("src") == kernel_source_hash():
+    rec = NCU_TRAFFIC.get((args.workload, family))
+    if rec and rec.get("src") == kernel_source_hash(family):
         traffic = rec["bytes"]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -391,7 +434,8 @@ def run_native(args, world: int, rank: int) -> dict | None:
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
-                     "kernel": "paged_decode_kernel (+ lse_combine when split)",
+                     "kernel": "shared_prefix_decode_kernel (+ plan and combine)" if shared
+                     else "paged_decode_kernel (+ lse_combine when split)",
                      "algorithmic_bytes_per_launch": ab["decode_launch"],
                      "decode_us_avg": round(dec_avg_s * 1e6, 2),
                      "decode_us_median": round(float(np.median(dec_ms)) * 1e3, 2)},
@@ -399,6 +443,8 @@ def run_native(args, world: int, rank: int) -> dict | None:
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3 / args.steps, 5)},
         "gpu_launches": launches_per_step * args.steps,
         "paging_overhead": paging,
+        "decode_path": "shared_prefix" if shared else "plain",
+        "plain_decode_comparison": plain_cmp,
         "clocks": clock_info,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -451,6 +497,9 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--decode", choices=["auto", "plain", "shared"], default="auto",
+                   help="decode entry point: auto = the shared-prefix kernel for batches "
+                        "with shared-prefix groups, the plain kernel otherwise")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-contiguous", action="store_true",
                    help="skip the contiguous-cache comparison")

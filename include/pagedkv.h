@@ -61,6 +61,8 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_FAULT_CONTEXT 4u   /* context_len < 0, > max_blocks_per_seq*block_size or
                                   > max_context_len: clamped */
 #define PKV_FAULT_TIMEOUT 8u   /* a shared-memory pipeline wait ran past its bound */
+#define PKV_FAULT_PREFIX 16u   /* a shared-prefix group description was inconsistent (see
+                                  pkv_paged_attention_decode_shared_prefix) */
 
 /* Flags of pkv_paged_attention_decode. */
 #define PKV_DECODE_PATH_AUTO 0  /* tensor cores when the GQA group makes dense tiles */
@@ -231,6 +233,53 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
                                            int max_context_len, float scale,
                                            int partition_tokens, void *workspace,
                                            size_t workspace_bytes, int flags, void *stream);
+
+/*
+ * Shared-prefix decode: the same result as pkv_paged_attention_decode for a
+ * batch in which groups of sequences share the physical blocks of a common
+ * prompt prefix (sequences forked from one prompt: parallel sampling, beam
+ * search; the Hacker News thread on PagedAttention describes such sharing of
+ * blocks between a sequence's siblings, and Qualiteg's "About PagedAttention
+ * for LLM serving" the per-sequence block tables that make it possible).
+ * Each shared block is read from HBM once per kv head for the whole group and
+ * multiplied against every member's query rows on tensor cores; each
+ * member's own blocks after the prefix are read as usual; a log-sum-exp pass
+ * merges the parts.
+ *
+ * Groups: group i is sequences group_starts[i] .. group_starts[i+1]-1, and
+ * every member's first prefix_lens[i] / block_size block-table entries name
+ * the same physical blocks.  group_starts: device int32 [num_groups + 1],
+ * non-decreasing from 0 to num_seqs (a sequence that shares nothing is a
+ * group of one).  prefix_lens: device int32 [num_groups], tokens, a multiple
+ * of the block size, at most max_prefix_len and at most every member's
+ * context length.  max_prefix_len: host bound used to size the workspace.
+ * The other arguments are those of pkv_paged_attention_decode; context_lens
+ * count every token, prefix included.
+ *
+ * A group description that breaks these rules (group_starts not covering the
+ * batch in order, a prefix length that is negative, not a whole number of
+ * blocks, above max_prefix_len or above a member's context, or members whose
+ * tables differ inside the prefix) sets PKV_FAULT_PREFIX.  Apart from table
+ * disagreement, which is only detected (the first member's blocks are used),
+ * the offending group is then computed without sharing, so the output is
+ * still exact.
+ *
+ * partition_tokens: 0 = automatic (prefix parts of 1024 tokens, per-sequence
+ * parts of 512), -1 = one part each, > 0 = parts of that many tokens (a
+ * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
+ * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
+ * holds the work list, so every call needs one.  Supported: bf16 pools,
+ * num_heads / num_kv_heads in 1..16, out_dtype F32 or BF16.
+ */
+size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                         int max_context_len, int max_prefix_len,
+                                         int partition_tokens);
+pkv_status pkv_paged_attention_decode_shared_prefix(
+    const pkv_pool *pool, void *out, pkv_dtype out_dtype, const void *query, int num_seqs,
+    int num_heads, int num_kv_heads, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, float scale, const int32_t *group_starts,
+    const int32_t *prefix_lens, int num_groups, int max_prefix_len, int partition_tokens,
+    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Copy whole physical blocks (every kv head, K and V): block dst[i] becomes a

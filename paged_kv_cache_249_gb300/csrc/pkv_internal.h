@@ -14,6 +14,7 @@ constexpr uint32_t kPoolMagic = 0x504b5631u;  // "PKV1"
 constexpr int kAutoPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 8192;
 constexpr int kMaxGroup = 16;
+constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 
 // Arguments of one decode launch; every pointer is a device pointer.
 struct DecodeArgs {
@@ -49,6 +50,53 @@ struct DecodeLaunch {
     cudaStream_t stream;
     int device;
 };
+
+// One work item of the shared-prefix decode, written by the planning kernel.
+struct SpEntry {
+    int seq0;      // first sequence of the item's query rows
+    int nseq;      // sequences in the item (rows = nseq * group)
+    int tbl_seq;   // sequence whose block-table row names the item's blocks
+    int b0, b1;    // logical blocks [b0, b1)
+    int slot;      // partial slot (of every row's sequence) the item writes
+    int tok_end;   // context positions >= tok_end are masked
+    int check;     // 1: check that the members' tables agree on [b0, b1)
+};
+static_assert(sizeof(SpEntry) == 32, "work item is two 16-byte words");
+
+// Arguments of the persistent shared-prefix decode kernel.
+struct SpArgs {
+    const void *q;              // [S][H][D] bf16
+    void *out;                  // [S][H][D] fp32 or bf16
+    float *ws_o;                // [S][H][num_slots][D] partial outputs
+    float *ws_lse;              // [S][H][num_slots] their log2-sum-exp
+    const int32_t *block_tables;
+    int32_t *dev_error;
+    const SpEntry *entries;     // work list (planning kernel)
+    const int32_t *nparts;      // [S] partials of each sequence (planning kernel)
+    int32_t *counter;           // work counter, zeroed by the planning kernel
+    const int32_t *count;       // number of entries (planning kernel)
+    int num_heads;
+    int num_kv_heads;
+    int group;
+    int max_blocks_per_seq;
+    int num_blocks;
+    int num_slots;
+    int out_bf16;
+    float scale_log2;
+};
+
+struct SpLaunch {
+    const CUtensorMap *tmk;
+    const CUtensorMap *tmv;
+    SpArgs args;
+    int head_dim;
+    int block_size;
+    cudaStream_t stream;
+    int device;
+};
+
+pkv_status launch_shared_prefix_d64(const SpLaunch &L);
+pkv_status launch_shared_prefix_d128(const SpLaunch &L);
 
 pkv_status launch_decode_f32_d64(const DecodeLaunch &L);
 pkv_status launch_decode_f32_d128(const DecodeLaunch &L);

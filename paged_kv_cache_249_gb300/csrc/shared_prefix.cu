@@ -1,0 +1,405 @@
+// shared_prefix.cu -- pkv_paged_attention_decode_shared_prefix: planning
+// kernel (work list from the group description), the log-sum-exp combine of
+// the per-item partials, and the host entry point.  The persistent decode
+// kernel itself is in shared_prefix_kernel.cuh.
+#include <math_constants.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kAutoPrefixPartition = 1024;  // tokens per prefix item (automatic)
+constexpr int kAutoSuffixPartition = 512;   // tokens per suffix item (automatic)
+constexpr int kPlanThreads = 1024;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Partition sizes in tokens (prefix, suffix) and the partial slots a sequence
+// can need: ceil(max_prefix / ptp) + ceil(max_context / pts).
+struct SpSizes {
+    int ptp, pts;      // tokens; -1 = one part
+    int slots;
+};
+
+SpSizes sp_sizes(int partition_tokens, int max_context_len, int max_prefix_len) {
+    SpSizes z;
+    const int maxp = max_prefix_len < max_context_len ? max_prefix_len : max_context_len;
+    int pp, ps;
+    if (partition_tokens < 0) {
+        z.ptp = z.pts = -1;
+        pp = maxp > 0 ? 1 : 0;
+        ps = max_context_len > 0 ? 1 : 0;
+    } else {
+        z.ptp = partition_tokens > 0 ? partition_tokens : kAutoPrefixPartition;
+        z.pts = partition_tokens > 0 ? partition_tokens : kAutoSuffixPartition;
+        pp = (maxp + z.ptp - 1) / z.ptp;
+        ps = (max_context_len + z.pts - 1) / z.pts;
+    }
+    z.slots = pp + ps > 0 ? pp + ps : 1;
+    return z;
+}
+
+struct SpLayout {
+    size_t header, nparts, entries, lse, o, total;
+};
+
+SpLayout sp_layout(int num_seqs, int num_heads, int head_dim, int slots) {
+    SpLayout L;
+    const size_t S = (size_t)num_seqs, rows = S * num_heads * slots;
+    L.header = 0;
+    L.nparts = 256;
+    L.entries = L.nparts + round_up(S * 4, 256);
+    L.lse = L.entries + round_up(S * slots * sizeof(SpEntry), 256);
+    L.o = L.lse + round_up(rows * 4, 256);
+    L.total = L.o + round_up(rows * head_dim * 4, 256);
+    return L;
+}
+
+// ------------------------------------------------------------ planning
+
+struct SpPlan {
+    const int32_t *group_starts;
+    const int32_t *prefix_lens;
+    const int32_t *context_lens;
+    int32_t *dev_error;
+    SpEntry *entries;
+    int32_t *nparts;
+    int32_t *header;        // [0] entries written, [1] work counter
+    int num_groups, num_seqs;
+    int ctx_cap;            // context lengths are clamped to [0, ctx_cap]
+    int max_prefix_len;     // tokens (already capped by max_context_len)
+    int block_size;
+    int pbp, pbs;           // blocks per prefix / suffix item
+    int members_per_item;   // floor(32 / group)
+    int max_entries;
+};
+
+__device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+// Members [start, end) of group i and the blocks they share (0 = none).
+// `flat`: the group description was rejected, every sequence is its own group.
+__device__ void sp_group(const SpPlan &p, bool flat, int i, bool report, int &start, int &end,
+                         int &pblk) {
+    pblk = 0;
+    if (flat) {
+        start = i;
+        end = i + 1;
+        return;
+    }
+    start = __ldg(p.group_starts + i);
+    end = __ldg(p.group_starts + i + 1);
+    const int plen = __ldg(p.prefix_lens + i);
+    if (plen == 0) return;
+    bool ok = plen > 0 && plen % p.block_size == 0 && plen <= p.max_prefix_len;
+    for (int s = start; ok && s < end; ++s)
+        ok = plen <= clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
+    if (!ok) {
+        if (report) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+        return;
+    }
+    if (end - start >= 2) pblk = plen / p.block_size;  // one member: nothing to share
+}
+
+// Exclusive block-wide scan of two counters (blockDim.x == kPlanThreads).
+__device__ void scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
+    __shared__ int wa[32], wb[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, ia, off);
+        const int xb = __shfl_up_sync(0xffffffffu, ib, off);
+        if (lane >= off) {
+            ia += xa;
+            ib += xb;
+        }
+    }
+    if (lane == 31) {
+        wa[warp] = ia;
+        wb[warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int va = wa[lane], vb = wb[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int xa = __shfl_up_sync(0xffffffffu, va, off);
+            const int xb = __shfl_up_sync(0xffffffffu, vb, off);
+            if (lane >= off) {
+                va += xa;
+                vb += xb;
+            }
+        }
+        wa[lane] = va;
+        wb[lane] = vb;
+    }
+    __syncthreads();
+    const int pa = warp > 0 ? wa[warp - 1] : 0, pb = warp > 0 ? wb[warp - 1] : 0;
+    ea = pa + ia - a;
+    eb = pb + ib - b;
+    ta = wa[31];
+    tb = wb[31];
+    __syncthreads();  // wa/wb are reused by the next call
+}
+
+// One CTA turns the group description into the work list: for every group
+// with a shared prefix, ceil(members / members_per_item) x ceil(prefix
+// blocks / pbp) prefix items; for every sequence, ceil(own blocks / pbs)
+// suffix items.  Prefix items come first (they are the largest), so the
+// persistent kernel's dynamic schedule ends on small items.
+__global__ void __launch_bounds__(kPlanThreads) shared_prefix_plan_kernel(const SpPlan p) {
+    const int tid = threadIdx.x;
+    bool bad = false;
+    for (int i = tid; i <= p.num_groups; i += blockDim.x) {
+        const int v = __ldg(p.group_starts + i);
+        if (v < 0 || v > p.num_seqs) bad = true;
+        if (i == 0 && v != 0) bad = true;
+        if (i == p.num_groups && v != p.num_seqs) bad = true;
+        if (i < p.num_groups && v > __ldg(p.group_starts + i + 1)) bad = true;
+    }
+    const bool flat = __syncthreads_or(bad);
+    if (flat && tid == 0) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+    for (int s = tid; s < p.num_seqs; s += blockDim.x) {
+        const int c = __ldg(p.context_lens + s);
+        if (c < 0 || c > p.ctx_cap) raise_fault(p.dev_error, PKV_FAULT_CONTEXT);
+    }
+    const int ngr = flat ? p.num_seqs : p.num_groups;
+    const int BS = p.block_size, mpi = p.members_per_item;
+
+    int total_pre = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        int run_pre = 0, run_suf = 0;
+#pragma unroll 1
+        for (int base = 0; base < ngr; base += blockDim.x) {
+            const int i = base + tid;
+            int start = 0, end = 0, pblk = 0, npre = 0, nsuf = 0, pp = 0;
+            if (i < ngr) {
+                sp_group(p, flat, i, pass == 0, start, end, pblk);
+                pp = (pblk + p.pbp - 1) / p.pbp;
+                npre = pp * ((end - start + mpi - 1) / mpi);
+                for (int s = start; s < end; ++s) {
+                    const int nb = (clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap) + BS - 1) / BS;
+                    nsuf += (nb - pblk + p.pbs - 1) / p.pbs;
+                }
+            }
+            int ep, es, tp, ts;
+            scan2(npre, nsuf, ep, es, tp, ts);
+            if (pass == 1 && i < ngr) {
+                int e = run_pre + ep;
+                for (int m0 = start; m0 < end && pp > 0; m0 += mpi) {
+                    const int nm = min(mpi, end - m0);
+                    for (int q = 0; q < pp; ++q, ++e) {
+                        if (e >= p.max_entries) {
+                            raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                            continue;
+                        }
+                        const int b0 = q * p.pbp, b1 = min(pblk, b0 + p.pbp);
+                        p.entries[e] = SpEntry{m0, nm, start, b0, b1, q, b1 * BS, nm > 1 ? 1 : 0};
+                    }
+                }
+                int f = total_pre + run_suf + es;
+                for (int s = start; s < end; ++s) {
+                    const int ctx = clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
+                    const int nb = (ctx + BS - 1) / BS;
+                    int nq = 0;
+                    for (int b0 = pblk; b0 < nb; b0 += p.pbs, ++nq, ++f) {
+                        if (f >= p.max_entries) {
+                            raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                            continue;
+                        }
+                        p.entries[f] = SpEntry{s, 1, s, b0, min(nb, b0 + p.pbs), pp + nq, ctx, 0};
+                    }
+                    p.nparts[s] = pp + nq;
+                }
+            }
+            run_pre += tp;
+            run_suf += ts;
+        }
+        if (pass == 0) total_pre = run_pre;
+        if (pass == 1 && tid == 0) {
+            const int n = total_pre + run_suf;
+            p.header[0] = n < p.max_entries ? n : p.max_entries;
+            p.header[1] = 0;
+        }
+    }
+}
+
+// ------------------------------------------------------------- combine
+
+// One warp per (sequence, head): sequences with one part were written by the
+// decode kernel; zero parts (empty context) give a zero row; otherwise
+// out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M), M = max_p lse_p.
+template <int D>
+__global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs a, int num_seqs) {
+    constexpr int PER = D / 32;
+    const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (wid >= num_seqs * a.num_heads) return;
+    const int s = wid / a.num_heads;
+    const int np = __ldg(a.nparts + s);
+    if (np == 1) return;
+    float res[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) res[j] = 0.f;
+    if (np > 1) {
+        const float *lse = a.ws_lse + (size_t)wid * a.num_slots;
+        const float *po = a.ws_o + (size_t)wid * a.num_slots * D + lane * PER;
+        float M = -CUDART_INF_F;
+        for (int q = lane; q < np; q += 32) M = fmaxf(M, lse[q]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M != -CUDART_INF_F) {
+            float den = 0.f, num[PER];
+#pragma unroll
+            for (int j = 0; j < PER; ++j) num[j] = 0.f;
+            for (int q = 0; q < np; ++q) {
+                const float w = fast_exp2(lse[q] - M);
+                den += w;
+                const float *v = po + (size_t)q * D;
+#pragma unroll
+                for (int j = 0; j < PER; ++j) num[j] = fmaf(w, v[j], num[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < PER; ++j) res[j] = den > 0.f ? num[j] / den : 0.f;
+        }
+    }
+    const size_t oi = (size_t)wid * D + lane * PER;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        if (a.out_bf16)
+            reinterpret_cast<__nv_bfloat16 *>(a.out)[oi + j] = __float2bfloat16_rn(res[j]);
+        else
+            reinterpret_cast<float *>(a.out)[oi + j] = res[j];
+    }
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                                    int max_context_len, int max_prefix_len,
+                                                    int partition_tokens) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        max_prefix_len < 0)
+        return 0;
+    const SpSizes z = sp_sizes(partition_tokens, max_context_len, max_prefix_len);
+    return sp_layout(num_seqs, num_heads, head_dim, z.slots).total;
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
+    const pkv_pool *pool, void *out, pkv_dtype out_dtype, const void *query, int num_seqs,
+    int num_heads, int num_kv_heads, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, float scale, const int32_t *group_starts,
+    const int32_t *prefix_lens, int num_groups, int max_prefix_len, int partition_tokens,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    if (!pool || pool->magic != kPoolMagic || pool->layout != 0) return PKV_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+        max_context_len < 0 || max_prefix_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_kv_heads != pool->num_kv_heads || num_heads % num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    const int BS = pool->block_size;
+    if (partition_tokens < -1 || partition_tokens > kMaxPartitionTokens ||
+        (partition_tokens > 0 && partition_tokens % BS != 0))
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (num_groups < 1 || num_groups > num_seqs) return PKV_ERR_INVALID_ARG;
+    if (!out || !query || !block_tables || !context_lens || !group_starts || !prefix_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(query, 16) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4) || !aligned(group_starts, 4) || !aligned(prefix_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    const int group = num_heads / num_kv_heads;
+    if (group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
+    if (dev != pool->device) return PKV_ERR_INVALID_ARG;
+
+    const SpSizes z = sp_sizes(partition_tokens, max_context_len, max_prefix_len);
+    const SpLayout lay = sp_layout(num_seqs, num_heads, pool->head_dim, z.slots);
+    if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+    const long long max_entries = (long long)num_seqs * z.slots;
+    if (max_entries * kMaxGroup * num_kv_heads >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+
+    const long long table_cap = (long long)max_blocks_per_seq * BS;
+    const int ctx_cap = (int)(table_cap < max_context_len ? table_cap : max_context_len);
+    const int maxp = max_prefix_len < max_context_len ? max_prefix_len : max_context_len;
+    const int cap_blocks = (ctx_cap + BS - 1) / BS;
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    SpPlan p;
+    std::memset(&p, 0, sizeof(p));
+    p.group_starts = group_starts;
+    p.prefix_lens = prefix_lens;
+    p.context_lens = context_lens;
+    p.dev_error = pool->dev_error;
+    p.entries = reinterpret_cast<SpEntry *>(ws + lay.entries);
+    p.nparts = reinterpret_cast<int32_t *>(ws + lay.nparts);
+    p.header = reinterpret_cast<int32_t *>(ws + lay.header);
+    p.num_groups = num_groups;
+    p.num_seqs = num_seqs;
+    p.ctx_cap = ctx_cap;
+    p.max_prefix_len = maxp;
+    p.block_size = BS;
+    p.pbp = z.ptp > 0 ? z.ptp / BS : ((maxp + BS - 1) / BS > 0 ? (maxp + BS - 1) / BS : 1);
+    p.pbs = z.pts > 0 ? z.pts / BS : (cap_blocks > 0 ? cap_blocks : 1);
+    p.members_per_item = kSpRowsMax / group;
+    p.max_entries = (int)max_entries;
+    shared_prefix_plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
+    if (cuda_status(cudaGetLastError()) != PKV_OK) return PKV_ERR_CUDA;
+
+    SpArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = query;
+    a.out = out;
+    a.ws_o = reinterpret_cast<float *>(ws + lay.o);
+    a.ws_lse = reinterpret_cast<float *>(ws + lay.lse);
+    a.block_tables = block_tables;
+    a.dev_error = pool->dev_error;
+    a.entries = p.entries;
+    a.nparts = p.nparts;
+    a.counter = p.header + 1;
+    a.count = p.header;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = group;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = pool->num_blocks;
+    a.num_slots = z.slots;
+    a.out_bf16 = out_dtype == PKV_BF16;
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    CUtensorMap maps[2];
+    std::memcpy(maps, pool->tma, sizeof(maps));
+    SpLaunch L;
+    L.tmk = &maps[0];
+    L.tmv = &maps[1];
+    L.args = a;
+    L.head_dim = pool->head_dim;
+    L.block_size = BS;
+    L.stream = st;
+    L.device = dev;
+    const pkv_status s1 =
+        pool->head_dim == 64 ? launch_shared_prefix_d64(L) : launch_shared_prefix_d128(L);
+    if (s1 != PKV_OK) return s1;
+
+    const unsigned nb = (unsigned)(((long long)num_seqs * num_heads + 7) / 8);
+    if (pool->head_dim == 64)
+        shared_prefix_combine_kernel<64><<<nb, 256, 0, st>>>(a, num_seqs);
+    else
+        shared_prefix_combine_kernel<128><<<nb, 256, 0, st>>>(a, num_seqs);
+    return cuda_status(cudaGetLastError());
+}

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 # pkv_dtype
 F32, BF16 = 0, 1
 # device fault bits
-FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT = 1, 2, 4, 8
+FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_PREFIX = 1, 2, 4, 8, 16
 # decode paths
 PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 
@@ -35,7 +35,8 @@ EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_bm_add_sequence", "pkv_bm_fork", "pkv_bm_append_token", "pkv_bm_free_sequence",
            "pkv_bm_context_len", "pkv_bm_pending_copies", "pkv_bm_take_copies",
            "pkv_bm_block_tables", "pkv_contiguous_cache_init",
-           "pkv_contiguous_attention_decode"]
+           "pkv_contiguous_attention_decode", "pkv_shared_prefix_workspace_bytes",
+           "pkv_paged_attention_decode_shared_prefix"]
 
 
 class PagedKVError(RuntimeError):
@@ -82,6 +83,9 @@ def load(path: Optional[str] = None):
         "pkv_copy_blocks": (I, [PP, P, P, I, P]),
         "pkv_contiguous_cache_init": (I, [PP, I, I, I, I, I, P, P, P, I, P]),
         "pkv_contiguous_attention_decode": (I, [PP, P, I, P, I, I, I, P, I, F, I, P, Z, I, P]),
+        "pkv_shared_prefix_workspace_bytes": (Z, [I, I, I, I, I, I]),
+        "pkv_paged_attention_decode_shared_prefix": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, P, P,
+                                                         I, I, I, P, Z, P]),
         "pkv_bm_create": (I, [I, I, ctypes.POINTER(P)]),
         "pkv_bm_destroy": (None, [P]),
         "pkv_bm_free_blocks": (I, [P]),
@@ -239,6 +243,37 @@ def paged_attention_decode_static(pool: BlockPool, out: torch.Tensor, query: tor
         int(partition_tokens), int(path), _stream(stream)), "pkv_paged_attention_decode_static")
 
 
+def shared_prefix_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int,
+                                  max_context_len: int, max_prefix_len: int,
+                                  partition_tokens: int = 0) -> int:
+    return load().pkv_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim,
+                                                    max_context_len, max_prefix_len,
+                                                    partition_tokens)
+
+
+def paged_attention_decode_shared_prefix(pool: BlockPool, out: torch.Tensor, query: torch.Tensor,
+                                         block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                         max_context_len: int, scale: float,
+                                         group_starts: torch.Tensor, prefix_lens: torch.Tensor,
+                                         max_prefix_len: int, workspace: torch.Tensor,
+                                         num_kv_heads: Optional[int] = None,
+                                         partition_tokens: int = 0, stream=None) -> None:
+    """pkv_paged_attention_decode_shared_prefix: decode for a batch whose
+    groups of sequences (group_starts, int32 [G+1]) share the blocks of a
+    prompt prefix (prefix_lens, int32 [G], tokens)."""
+    S, H, _ = query.shape
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert group_starts.dtype == torch.int32 and prefix_lens.dtype == torch.int32
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_attention_decode_shared_prefix(
+        ctypes.byref(pool.desc), out.data_ptr(), _dtype_code(out.dtype), query.data_ptr(), S, H,
+        num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), int(max_context_len), float(scale),
+        group_starts.data_ptr(), prefix_lens.data_ptr(), prefix_lens.numel(),
+        int(max_prefix_len), int(partition_tokens), workspace.data_ptr(), ws_bytes,
+        _stream(stream)), "pkv_paged_attention_decode_shared_prefix")
+
+
 class ContiguousCache:
     """A conventional [S][Hkv][capacity][D] K/V cache (the layout a paged
     pool replaces), described to the library for the paging-overhead
@@ -392,6 +427,7 @@ class DeviceWorkload:
         self.block_tables = torch.from_numpy(w.block_tables).to(device)
         self.context_lens = torch.from_numpy(w.context_lens).to(device)
         self.slot_mapping = torch.from_numpy(w.slot_mapping).to(device)
+        self.device = device
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=device)
         self.pool = BlockPool(self.k_pool, self.v_pool, self.dev_error)
         self.out = torch.empty(w.num_seqs, w.num_heads, w.head_dim,
@@ -410,3 +446,28 @@ class DeviceWorkload:
         paged_attention_decode(self.pool, self.out, self.q, self.block_tables, self.context_lens,
                                self.max_context_len, self.w.scale, self.w.num_kv_heads,
                                self.partition_tokens, self.workspace, path, stream)
+
+    def shared_prefix_setup(self, partition_tokens: int = 0, group_starts=None,
+                            prefix_lens=None, max_prefix_len: Optional[int] = None) -> None:
+        """Upload the batch's group description (or the one given) and size the
+        shared-prefix workspace."""
+        gs, gp = self.w.groups()
+        gs = gs if group_starts is None else np.asarray(group_starts, dtype=np.int32)
+        gp = gp if prefix_lens is None else np.asarray(prefix_lens, dtype=np.int32)
+        self.group_starts = torch.from_numpy(np.ascontiguousarray(gs)).to(self.device)
+        self.prefix_lens = torch.from_numpy(np.ascontiguousarray(gp)).to(self.device)
+        self.max_prefix_len = int(max_prefix_len if max_prefix_len is not None else
+                                  (max(0, int(gp.max())) if gp.size else 0))
+        self.sp_partition = partition_tokens
+        n = shared_prefix_workspace_bytes(self.w.num_seqs, self.w.num_heads, self.w.head_dim,
+                                          self.max_context_len, self.max_prefix_len,
+                                          partition_tokens)
+        self.sp_workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+
+    def decode_shared_prefix(self, stream=None) -> None:
+        if not hasattr(self, "sp_workspace"):
+            self.shared_prefix_setup()
+        paged_attention_decode_shared_prefix(
+            self.pool, self.out, self.q, self.block_tables, self.context_lens,
+            self.max_context_len, self.w.scale, self.group_starts, self.prefix_lens,
+            self.max_prefix_len, self.sp_workspace, self.w.num_kv_heads, self.sp_partition, stream)

@@ -66,8 +66,10 @@ class Workload:
     v_pool: torch.Tensor
     new_key: torch.Tensor      # [S][Hkv][D] (CPU)
     new_value: torch.Tensor
-    group_size: int = 1        # sequences per shared-prefix group (1 = none)
-    prefix_len: int = 0        # shared-prefix tokens per group
+    group_size: int = 1        # sequences per shared-prefix group (1 = none; uniform groups)
+    prefix_len: int = 0        # shared-prefix tokens per group (uniform groups)
+    group_starts: Optional[np.ndarray] = None  # int32 [G+1]: group i = seqs [gs[i], gs[i+1])
+    group_prefix: Optional[np.ndarray] = None  # int32 [G]: tokens group i shares
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -88,11 +90,21 @@ class Workload:
 
     def kv_bytes_unique(self) -> int:
         """K+V bytes of distinct physical tokens (shared prefixes once)."""
-        if self.group_size <= 1:
-            return self.kv_bytes_logical()
+        gs, gp = self.groups()
         ctx = self.context_lens.astype(np.int64)
-        uniq = ctx.sum() - (self.group_size - 1) * (self.num_seqs // self.group_size) * self.prefix_len
+        uniq = ctx.sum() - int(np.sum((np.diff(gs).astype(np.int64) - 1).clip(min=0) *
+                                      gp.astype(np.int64)))
         return int(uniq) * self.num_kv_heads * self.head_dim * 2 * self.elem_bytes
+
+    def groups(self) -> tuple[np.ndarray, np.ndarray]:
+        """(group_starts int32 [G+1], prefix tokens int32 [G]) of the batch;
+        a batch without sharing is one group per sequence with no prefix."""
+        if self.group_starts is not None:
+            return self.group_starts, self.group_prefix
+        if self.group_size > 1:
+            gs = np.arange(0, self.num_seqs + 1, self.group_size, dtype=np.int32)
+            return gs, np.full(gs.size - 1, self.prefix_len, dtype=np.int32)
+        return np.arange(self.num_seqs + 1, dtype=np.int32), np.zeros(self.num_seqs, np.int32)
 
 
 def _normal_f32(ss: np.random.SeedSequence, n: int, threads: int = 0) -> np.ndarray:
@@ -129,7 +141,8 @@ def build(name: str, *, dtype: str, context_lens: Sequence[int], num_heads: int,
           meta_seed: int, placement: str = "shuffle", pool_blocks: Optional[int] = None,
           max_blocks_per_seq: Optional[int] = None, partition_tokens: int = 0,
           group_size: int = 1, prefix_len: int = 0, scale: Optional[float] = None,
-          tail_fill: Optional[float] = None) -> Workload:
+          tail_fill: Optional[float] = None,
+          groups: Optional[Sequence[tuple[int, int]]] = None) -> Workload:
     """Lay out a paged workload and fill it with seeded N(0,1) data.
 
     placement: "shuffle" (seeded permutation of the pool), "identity"
@@ -137,24 +150,37 @@ def build(name: str, *, dtype: str, context_lens: Sequence[int], num_heads: int,
     group_size/prefix_len: consecutive groups of ``group_size`` sequences
     share the physical blocks of their first ``prefix_len`` tokens
     (prefix_len must be a multiple of block_size).
+    groups: ragged alternative, a list of (members, prefix_len): consecutive
+    sequences form the groups in order (members summing to the batch).
     tail_fill: if given, every pool slot that no context position maps to is
     set to this value (e.g. NaN), to check that masked slots are ignored.
     """
     ctx = np.asarray(context_lens, dtype=np.int64)
     S = int(ctx.size)
     BS = block_size
-    if group_size > 1:
-        assert S % group_size == 0 and prefix_len % BS == 0
-        assert np.all(ctx >= prefix_len)
+    if groups is None:
+        if group_size > 1:
+            assert S % group_size == 0
+            groups = [(group_size, prefix_len)] * (S // group_size)
+        else:
+            groups = [(1, 0)] * S
+    sizes = np.array([m for m, _ in groups], dtype=np.int64)
+    gpref = np.array([p for _, p in groups], dtype=np.int64)
+    assert int(sizes.sum()) == S and np.all(sizes >= 1) and np.all(gpref % BS == 0)
+    gstart = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    seq_group = np.repeat(np.arange(len(groups)), sizes)
+    for gi in range(len(groups)):
+        assert np.all(ctx[gstart[gi]:gstart[gi + 1]] >= gpref[gi])
     nblk = (ctx + BS - 1) // BS
-    shared = prefix_len // BS if group_size > 1 else 0
+    gshared = np.where(sizes > 1, gpref // BS, 0)
     # unique logical blocks: per group the shared prefix once, then each
     # sequence's own blocks after the prefix
     owners = []  # (seq or -group-1 marker, logical block) for each unique block
     for s in range(S):
-        if group_size > 1 and s % group_size == 0:
-            owners.extend(("p", s // group_size, b) for b in range(shared))
-        owners.extend(("s", s, b) for b in range(shared, int(nblk[s])))
+        gi = int(seq_group[s])
+        if s == gstart[gi]:
+            owners.extend(("p", gi, b) for b in range(int(gshared[gi])))
+        owners.extend(("s", s, b) for b in range(int(gshared[gi]), int(nblk[s])))
     n_unique = len(owners)
     NB = int(pool_blocks) if pool_blocks is not None else n_unique
     assert NB >= n_unique
@@ -177,8 +203,9 @@ def build(name: str, *, dtype: str, context_lens: Sequence[int], num_heads: int,
         else:
             bt[a, b] = int(perm[i])
     for s in range(S):
-        for b in range(shared):
-            bt[s, b] = prefix_phys[(s // group_size, b)]
+        gi = int(seq_group[s])
+        for b in range(int(gshared[gi])):
+            bt[s, b] = prefix_phys[(gi, b)]
     slot = np.full(S, -1, dtype=np.int64)
     for s in range(S):
         if ctx[s] > 0:
@@ -206,7 +233,8 @@ def build(name: str, *, dtype: str, context_lens: Sequence[int], num_heads: int,
         scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
         partition_tokens=partition_tokens, context_lens=ctx.astype(np.int32), block_tables=bt,
         slot_mapping=slot, q=q, k_pool=k_pool, v_pool=v_pool, new_key=nk, new_value=nv,
-        group_size=group_size, prefix_len=prefix_len if group_size > 1 else 0)
+        group_size=group_size, prefix_len=prefix_len if group_size > 1 else 0,
+        group_starts=gstart.astype(np.int32), group_prefix=np.where(sizes > 1, gpref, 0).astype(np.int32))
 
 
 # The five decode workloads, by name. Sizes follow the PagedAttention decode
@@ -274,4 +302,5 @@ def subset(w: Workload, seqs: Sequence[int]) -> Workload:
         w, num_seqs=int(idx.size), context_lens=w.context_lens[idx].copy(),
         block_tables=w.block_tables[idx].copy(), slot_mapping=w.slot_mapping[idx].copy(),
         q=w.q[torch.from_numpy(idx)].contiguous(), new_key=w.new_key[torch.from_numpy(idx)].contiguous(),
-        new_value=w.new_value[torch.from_numpy(idx)].contiguous(), group_size=1, prefix_len=0)
+        new_value=w.new_value[torch.from_numpy(idx)].contiguous(), group_size=1, prefix_len=0,
+        group_starts=None, group_prefix=None)

@@ -1,0 +1,172 @@
+"""The shared-prefix decode (pkv_paged_attention_decode_shared_prefix) against
+the float64 oracle.
+
+Sequences forked from one prompt share the prompt's physical blocks (the
+Hacker News thread on PagedAttention; Qualiteg's per-sequence block tables):
+the attention result is the same as for private copies, which the oracle
+computes by gathering each sequence's blocks through its own table.  The
+cases cover ragged groups, every GQA group size the kernel packs (1 to 16
+query heads per KV head, with members split across 32-row work items),
+empty suffixes, partial last blocks, both head sizes and block sizes, both
+output types, and group descriptions that break the rules (reported in the
+error word; the output must still be exact).
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_249_gb300 import pagedkv, workload
+from tests.gpu_helpers import assert_close, oracle_after_write
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(name, ctx, groups, H, Hkv, D=128, BS=16, seed=0, **kw):
+    return workload.build(name, dtype="bf16", context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
+                          head_dim=D, block_size=BS, data_seed=5000 + seed,
+                          meta_seed=6000 + seed, groups=groups, **kw)
+
+
+def _run(w, partition=0, out_dtype=torch.float32, **setup):
+    dw = pagedkv.DeviceWorkload(w, out_dtype=out_dtype)
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    dw.shared_prefix_setup(partition_tokens=partition, **setup)
+    dw.decode_shared_prefix()
+    torch.cuda.synchronize()
+    return dw
+
+
+def _prefix_ctx(prefix, suffixes):
+    return [prefix + s for s in suffixes]
+
+
+CASES = {
+    # name: (context lengths, groups, H, Hkv, D, BS)
+    "g4_eight_members": (_prefix_ctx(256, [0, 1, 15, 16, 17, 100, 300, 700]), [(8, 256)],
+                         32, 8, 128, 16),
+    "g4_ragged_groups": ([70, 64, 100, 5, 130, 128, 300, 129, 200, 40, 33],
+                         [(3, 64), (1, 0), (5, 128), (2, 32)], 16, 4, 128, 16),
+    "mha_g1": (_prefix_ctx(512, [3, 40, 90, 0, 17, 600]), [(6, 512)], 8, 8, 128, 16),
+    "g8_two_items": (_prefix_ctx(320, [1, 2, 3, 50, 60, 200]), [(6, 320)], 64, 8, 128, 16),
+    "g16_pairs": (_prefix_ctx(160, [9, 0, 31]), [(3, 160)], 16, 1, 128, 16),
+    "g3_odd": (_prefix_ctx(96, list(range(0, 130, 13))), [(10, 96)], 6, 2, 128, 16),
+    "d64_bs32": (_prefix_ctx(384, [5, 64, 33, 1]), [(2, 384), (2, 96)], 8, 2, 64, 32),
+    "d128_bs32": (_prefix_ctx(640, [31, 32, 33, 500]), [(4, 640)], 16, 4, 128, 32),
+    "d64_bs16_mha": (_prefix_ctx(48, [1, 2, 3]), [(3, 48)], 4, 4, 64, 16),
+    "big_group": (_prefix_ctx(1024, list(range(1, 40 * 7, 7))), [(40, 1024)], 8, 8, 128, 16),
+}
+
+
+@pytest.mark.parametrize("partition", [0, -1, 64])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_shared_prefix_matches_oracle(case, partition):
+    ctx, groups, H, Hkv, D, BS = CASES[case]
+    if partition > 0 and partition % BS:
+        partition = BS * 4
+    w = _w(case, ctx, groups, H, Hkv, D, BS, seed=sorted(CASES).index(case))
+    ref, _, _ = oracle_after_write(w)
+    dw = _run(w, partition)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "bf16", f"{case} partition {partition}")
+
+
+@pytest.mark.parametrize("case", ["g4_eight_members", "g4_ragged_groups", "d64_bs32"])
+def test_shared_prefix_bf16_output(case):
+    ctx, groups, H, Hkv, D, BS = CASES[case]
+    w = _w(case, ctx, groups, H, Hkv, D, BS, seed=3)
+    ref, _, _ = oracle_after_write(w)
+    dw = _run(w, 0, torch.bfloat16)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "bf16", f"{case} bf16 output")
+
+
+def test_no_sharing_and_empty_contexts():
+    """Groups of one (nothing shared), including zero-length contexts."""
+    ctx = [0, 1, 17, 0, 900, 2048, 5]
+    w = _w("flat", ctx, [(1, 0)] * len(ctx), 32, 8, seed=11)
+    ref, _, _ = oracle_after_write(w)
+    for pt in (0, 256, -1):
+        dw = _run(w, pt)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, "bf16", f"flat partition {pt}")
+    assert float(dw.out[0].abs().max()) == 0.0 and float(dw.out[3].abs().max()) == 0.0
+
+
+def test_repeat_calls_are_bitwise_equal():
+    ctx, groups, H, Hkv, D, BS = CASES["g4_ragged_groups"]
+    w = _w("rep", ctx, groups, H, Hkv, D, BS, seed=12)
+    dw = _run(w, 64)
+    first = dw.out.clone()
+    for _ in range(3):
+        dw.decode_shared_prefix()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int32), dw.out.view(torch.int32))
+
+
+def test_agrees_with_the_plain_decode():
+    ctx, groups, H, Hkv, D, BS = CASES["g8_two_items"]
+    w = _w("plain", ctx, groups, H, Hkv, D, BS, seed=13)
+    sp = _run(w, 0)
+    plain = pagedkv.DeviceWorkload(w)
+    plain.step()
+    torch.cuda.synchronize()
+    assert float((sp.out - plain.out).abs().max()) <= 4e-3
+
+
+# ------------------------------------------------ broken group descriptions
+
+def _broken(setup, expect_exact=True):
+    ctx = _prefix_ctx(256, [20, 30, 300, 5, 0, 64])
+    w = _w("broken", ctx, [(3, 256), (3, 256)], 16, 4, seed=14)
+    ref, _, _ = oracle_after_write(w)
+    dw = _run(w, 0, **setup)
+    bits = pagedkv.get_device_error(dw.pool)
+    assert bits & pagedkv.FAULT_PREFIX, bits
+    if expect_exact:
+        assert_close(dw.out, ref, "bf16", f"fallback after {setup}")
+
+
+def test_group_starts_not_covering_the_batch():
+    _broken(dict(group_starts=[0, 4, 3, 6], prefix_lens=[256, 256, 0]))
+    _broken(dict(group_starts=[0, 3, 5], prefix_lens=[256, 256]))
+
+
+def test_prefix_longer_than_a_member():
+    _broken(dict(prefix_lens=[256, 512], max_prefix_len=512))
+
+
+def test_prefix_not_whole_blocks():
+    _broken(dict(prefix_lens=[250, 256]))
+
+
+def test_prefix_above_host_bound():
+    _broken(dict(prefix_lens=[256, 256], max_prefix_len=128))
+
+
+def test_prefix_negative():
+    _broken(dict(prefix_lens=[-16, 256]))
+
+
+def test_tables_that_differ_inside_the_prefix_are_reported():
+    # members share 256 tokens, the description claims 272 (one block more)
+    _broken(dict(prefix_lens=[272, 256], max_prefix_len=272), expect_exact=False)
+
+
+# --------------------------------------------------------------- full size
+
+def test_fullsize_shared_prefix_workload_sampled():
+    w = workload.make("shared_prefix")
+    dw = pagedkv.DeviceWorkload(w, out_dtype=torch.bfloat16)
+    dw.step()  # cache write + plain decode
+    torch.cuda.synchronize()
+    plain = dw.out.clone()
+    dw.decode_shared_prefix()
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw.pool) == 0
+    rng = np.random.default_rng(4)
+    seqs = sorted({0, 1, 7, 8, w.num_seqs - 1, *rng.integers(0, w.num_seqs, 5).tolist()})
+    ref, _, _ = oracle_after_write(w, seqs)
+    assert_close(dw.out[torch.tensor(seqs, device=dw.out.device)], ref, "bf16",
+                 "shared_prefix workload")
+    # every sequence agrees with the plain kernel to within both tolerances
+    assert float((dw.out.float() - plain.float()).abs().max()) <= 4e-3 + 2 ** -8
