@@ -260,9 +260,9 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * batch in order, a prefix length that is negative, not a whole number of
  * blocks, above max_prefix_len or above a member's context, or members whose
  * tables differ inside the prefix) sets PKV_FAULT_PREFIX.  Apart from table
- * disagreement, which is only detected (the first member's blocks are used),
- * the offending group is then computed without sharing, so the output is
- * still exact.
+ * disagreement, which is only detected (after the fact: the first member's
+ * blocks are used), the offending group is then computed without sharing,
+ * so the output is still exact.
  *
  * partition_tokens: 0 = automatic (prefix parts of 1024 tokens, per-sequence
  * parts of 512), -1 = one part each, > 0 = parts of that many tokens (a

@@ -59,7 +59,7 @@ struct SpEntry {
     int b0, b1;    // logical blocks [b0, b1)
     int slot;      // partial slot (of every row's sequence) the item writes
     int tok_end;   // context positions >= tok_end are masked
-    int check;     // 1: check that the members' tables agree on [b0, b1)
+    int reserved;
 };
 static_assert(sizeof(SpEntry) == 32, "work item is two 16-byte words");
 
@@ -71,10 +71,14 @@ struct SpArgs {
     float *ws_lse;              // [S][H][num_slots] their log2-sum-exp
     const int32_t *block_tables;
     int32_t *dev_error;
-    const SpEntry *entries;     // work list (planning kernel)
+    const SpEntry *entries;     // work list: prefix items at [0, count[0]), suffix items at
+                                // [suffix_base, suffix_base + count[1]) (planning kernel)
     const int32_t *nparts;      // [S] partials of each sequence (planning kernel)
+    const int32_t *seq_share;   // [S][2] group leader and shared blocks (planning kernel)
+    const int32_t *block_tables_chk;  // block tables, for the combine's agreement check
     int32_t *counter;           // work counter, zeroed by the planning kernel
-    const int32_t *count;       // number of entries (planning kernel)
+    const int32_t *count;       // [2]: prefix and suffix entries (planning kernel)
+    int suffix_base;
     int num_heads;
     int num_kv_heads;
     int group;

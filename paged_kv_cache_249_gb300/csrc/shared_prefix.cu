@@ -13,7 +13,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kAutoPrefixPartition = 1024;  // tokens per prefix item (automatic)
+constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic)
 constexpr int kAutoSuffixPartition = 512;   // tokens per suffix item (automatic)
 constexpr int kPlanThreads = 1024;
 
@@ -24,6 +24,7 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // can need: ceil(max_prefix / ptp) + ceil(max_context / pts).
 struct SpSizes {
     int ptp, pts;      // tokens; -1 = one part
+    int pp, ps;        // most prefix / suffix parts of one sequence
     int slots;
 };
 
@@ -41,12 +42,14 @@ SpSizes sp_sizes(int partition_tokens, int max_context_len, int max_prefix_len) 
         pp = (maxp + z.ptp - 1) / z.ptp;
         ps = (max_context_len + z.pts - 1) / z.pts;
     }
+    z.pp = pp;
+    z.ps = ps;
     z.slots = pp + ps > 0 ? pp + ps : 1;
     return z;
 }
 
 struct SpLayout {
-    size_t header, nparts, entries, lse, o, total;
+    size_t header, nparts, share, entries, lse, o, total;
 };
 
 SpLayout sp_layout(int num_seqs, int num_heads, int head_dim, int slots) {
@@ -54,7 +57,8 @@ SpLayout sp_layout(int num_seqs, int num_heads, int head_dim, int slots) {
     const size_t S = (size_t)num_seqs, rows = S * num_heads * slots;
     L.header = 0;
     L.nparts = 256;
-    L.entries = L.nparts + round_up(S * 4, 256);
+    L.share = L.nparts + round_up(S * 4, 256);
+    L.entries = L.share + round_up(S * 8, 256);
     L.lse = L.entries + round_up(S * slots * sizeof(SpEntry), 256);
     L.o = L.lse + round_up(rows * 4, 256);
     L.total = L.o + round_up(rows * head_dim * 4, 256);
@@ -70,41 +74,19 @@ struct SpPlan {
     int32_t *dev_error;
     SpEntry *entries;
     int32_t *nparts;
-    int32_t *header;        // [0] entries written, [1] work counter
+    int32_t *share;         // [S][2]: group leader, shared blocks
+    int32_t *header;        // [0] prefix entries, [1] suffix entries, [2] work counter
     int num_groups, num_seqs;
     int ctx_cap;            // context lengths are clamped to [0, ctx_cap]
     int max_prefix_len;     // tokens (already capped by max_context_len)
     int block_size;
     int pbp, pbs;           // blocks per prefix / suffix item
     int members_per_item;   // floor(32 / group)
-    int max_entries;
+    int prefix_cap;         // entries [0, prefix_cap) hold prefix items
+    int suffix_cap;         // entries [prefix_cap, prefix_cap + suffix_cap) hold suffix items
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
-
-// Members [start, end) of group i and the blocks they share (0 = none).
-// `flat`: the group description was rejected, every sequence is its own group.
-__device__ void sp_group(const SpPlan &p, bool flat, int i, bool report, int &start, int &end,
-                         int &pblk) {
-    pblk = 0;
-    if (flat) {
-        start = i;
-        end = i + 1;
-        return;
-    }
-    start = __ldg(p.group_starts + i);
-    end = __ldg(p.group_starts + i + 1);
-    const int plen = __ldg(p.prefix_lens + i);
-    if (plen == 0) return;
-    bool ok = plen > 0 && plen % p.block_size == 0 && plen <= p.max_prefix_len;
-    for (int s = start; ok && s < end; ++s)
-        ok = plen <= clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
-    if (!ok) {
-        if (report) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-        return;
-    }
-    if (end - start >= 2) pblk = plen / p.block_size;  // one member: nothing to share
-}
 
 // Exclusive block-wide scan of two counters (blockDim.x == kPlanThreads).
 __device__ void scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
@@ -148,13 +130,23 @@ __device__ void scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
     __syncthreads();  // wa/wb are reused by the next call
 }
 
-// One CTA turns the group description into the work list: for every group
-// with a shared prefix, ceil(members / members_per_item) x ceil(prefix
-// blocks / pbp) prefix items; for every sequence, ceil(own blocks / pbs)
-// suffix items.  Prefix items come first (they are the largest), so the
-// persistent kernel's dynamic schedule ends on small items.
-__global__ void __launch_bounds__(kPlanThreads) shared_prefix_plan_kernel(const SpPlan p) {
+// One CTA turns the group description into the work list in one pass over
+// the groups: for every group with a shared prefix, ceil(members /
+// members_per_item) x ceil(prefix blocks / pbp) prefix items; for every
+// sequence, ceil(own blocks / pbs) suffix items.  Prefix items (the largest)
+// and suffix items go to separate regions; the decode kernel takes all
+// prefix items first, so its dynamic schedule ends on small items.  Context
+// lengths are staged in shared memory first (one parallel round trip), so
+// the per-group loops over members touch no global memory.
+constexpr int kPlanSmemSeqs = 8192;
+
+__global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(const SpPlan p) {
+    __shared__ int s_ctx[kPlanSmemSeqs];
+    // the decode kernel may start setting up; it waits for this grid in
+    // griddepcontrol.wait before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
+    const bool staged = p.num_seqs <= kPlanSmemSeqs;
     bool bad = false;
     for (int i = tid; i <= p.num_groups; i += blockDim.x) {
         const int v = __ldg(p.group_starts + i);
@@ -163,71 +155,88 @@ __global__ void __launch_bounds__(kPlanThreads) shared_prefix_plan_kernel(const 
         if (i == p.num_groups && v != p.num_seqs) bad = true;
         if (i < p.num_groups && v > __ldg(p.group_starts + i + 1)) bad = true;
     }
-    const bool flat = __syncthreads_or(bad);
-    if (flat && tid == 0) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
     for (int s = tid; s < p.num_seqs; s += blockDim.x) {
         const int c = __ldg(p.context_lens + s);
         if (c < 0 || c > p.ctx_cap) raise_fault(p.dev_error, PKV_FAULT_CONTEXT);
+        if (staged) s_ctx[s] = clamp_ctx(c, p.ctx_cap);
     }
+    const bool flat = __syncthreads_or(bad);
+    if (flat && tid == 0) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+    auto ctx_of = [&](int s) -> int {
+        return staged ? s_ctx[s] : clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
+    };
     const int ngr = flat ? p.num_seqs : p.num_groups;
     const int BS = p.block_size, mpi = p.members_per_item;
 
-    int total_pre = 0;
+    int run_pre = 0, run_suf = 0;
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        int run_pre = 0, run_suf = 0;
-#pragma unroll 1
-        for (int base = 0; base < ngr; base += blockDim.x) {
-            const int i = base + tid;
-            int start = 0, end = 0, pblk = 0, npre = 0, nsuf = 0, pp = 0;
-            if (i < ngr) {
-                sp_group(p, flat, i, pass == 0, start, end, pblk);
-                pp = (pblk + p.pbp - 1) / p.pbp;
-                npre = pp * ((end - start + mpi - 1) / mpi);
-                for (int s = start; s < end; ++s) {
-                    const int nb = (clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap) + BS - 1) / BS;
-                    nsuf += (nb - pblk + p.pbs - 1) / p.pbs;
+    for (int base = 0; base < ngr; base += blockDim.x) {
+        const int i = base + tid;
+        int start = 0, end = 0, pblk = 0, npre = 0, nsuf = 0, pp = 0;
+        if (i < ngr) {
+            // members [start, end) and the blocks they share (0 = none)
+            if (flat) {
+                start = i;
+                end = i + 1;
+            } else {
+                start = __ldg(p.group_starts + i);
+                end = __ldg(p.group_starts + i + 1);
+                const int plen = __ldg(p.prefix_lens + i);
+                if (plen != 0) {
+                    bool ok = plen > 0 && plen % BS == 0 && plen <= p.max_prefix_len;
+                    for (int s = start; ok && s < end; ++s) ok = plen <= ctx_of(s);
+                    if (!ok)
+                        raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                    else if (end - start >= 2)  // one member: nothing to share
+                        pblk = plen / BS;
                 }
             }
-            int ep, es, tp, ts;
-            scan2(npre, nsuf, ep, es, tp, ts);
-            if (pass == 1 && i < ngr) {
-                int e = run_pre + ep;
-                for (int m0 = start; m0 < end && pp > 0; m0 += mpi) {
-                    const int nm = min(mpi, end - m0);
-                    for (int q = 0; q < pp; ++q, ++e) {
-                        if (e >= p.max_entries) {
-                            raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-                            continue;
-                        }
-                        const int b0 = q * p.pbp, b1 = min(pblk, b0 + p.pbp);
-                        p.entries[e] = SpEntry{m0, nm, start, b0, b1, q, b1 * BS, nm > 1 ? 1 : 0};
+            pp = (pblk + p.pbp - 1) / p.pbp;
+            npre = pp * ((end - start + mpi - 1) / mpi);
+            for (int s = start; s < end; ++s) {
+                const int nb = (ctx_of(s) + BS - 1) / BS;
+                nsuf += (nb - pblk + p.pbs - 1) / p.pbs;
+            }
+        }
+        int ep, es, tp, ts;
+        scan2(npre, nsuf, ep, es, tp, ts);
+        if (i < ngr) {
+            int e = run_pre + ep;
+            for (int m0 = start; m0 < end && pp > 0; m0 += mpi) {
+                const int nm = min(mpi, end - m0);
+                for (int q = 0; q < pp; ++q, ++e) {
+                    if (e >= p.prefix_cap) {
+                        raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                        continue;
                     }
-                }
-                int f = total_pre + run_suf + es;
-                for (int s = start; s < end; ++s) {
-                    const int ctx = clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
-                    const int nb = (ctx + BS - 1) / BS;
-                    int nq = 0;
-                    for (int b0 = pblk; b0 < nb; b0 += p.pbs, ++nq, ++f) {
-                        if (f >= p.max_entries) {
-                            raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-                            continue;
-                        }
-                        p.entries[f] = SpEntry{s, 1, s, b0, min(nb, b0 + p.pbs), pp + nq, ctx, 0};
-                    }
-                    p.nparts[s] = pp + nq;
+                    const int b0 = q * p.pbp, b1 = min(pblk, b0 + p.pbp);
+                    p.entries[e] = SpEntry{m0, nm, start, b0, b1, q, b1 * BS, 0};
                 }
             }
-            run_pre += tp;
-            run_suf += ts;
+            int f = run_suf + es;
+            for (int s = start; s < end; ++s) {
+                const int ctx = ctx_of(s);
+                const int nb = (ctx + BS - 1) / BS;
+                int nq = 0;
+                for (int b0 = pblk; b0 < nb; b0 += p.pbs, ++nq, ++f) {
+                    if (f >= p.suffix_cap) {
+                        raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                        continue;
+                    }
+                    p.entries[p.prefix_cap + f] = SpEntry{s, 1, s, b0, min(nb, b0 + p.pbs), pp + nq, ctx, 0};
+                }
+                p.nparts[s] = pp + nq;
+                p.share[2 * s] = start;
+                p.share[2 * s + 1] = pblk;
+            }
         }
-        if (pass == 0) total_pre = run_pre;
-        if (pass == 1 && tid == 0) {
-            const int n = total_pre + run_suf;
-            p.header[0] = n < p.max_entries ? n : p.max_entries;
-            p.header[1] = 0;
-        }
+        run_pre += tp;
+        run_suf += ts;
+    }
+    if (tid == 0) {
+        p.header[0] = run_pre < p.prefix_cap ? run_pre : p.prefix_cap;
+        p.header[1] = run_suf < p.suffix_cap ? run_suf : p.suffix_cap;
+        p.header[2] = 0;
     }
 }
 
@@ -236,13 +245,26 @@ __global__ void __launch_bounds__(kPlanThreads) shared_prefix_plan_kernel(const 
 // One warp per (sequence, head): sequences with one part were written by the
 // decode kernel; zero parts (empty context) give a zero row; otherwise
 // out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M), M = max_p lse_p.
+// Launched as a programmatic dependent of the decode kernel.
 template <int D>
 __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs a, int num_seqs) {
     constexpr int PER = D / 32;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (wid >= num_seqs * a.num_heads) return;
     const int s = wid / a.num_heads;
-    const int np = __ldg(a.nparts + s);
+    const int np = a.nparts[s];
+    if (wid % a.num_heads == 0) {
+        // members must name their leader's blocks inside the shared prefix
+        const int leader = a.seq_share[2 * s], pblk = a.seq_share[2 * s + 1];
+        if (pblk > 0 && leader != s) {
+            const int32_t *mine = a.block_tables_chk + (size_t)s * a.max_blocks_per_seq;
+            const int32_t *lead = a.block_tables_chk + (size_t)leader * a.max_blocks_per_seq;
+            bool bad = false;
+            for (int b = lane; b < pblk; b += 32) bad |= __ldg(mine + b) != __ldg(lead + b);
+            if (__any_sync(0xffffffffu, bad) && lane == 0) raise_fault(a.dev_error, PKV_FAULT_PREFIX);
+        }
+    }
     if (np == 1) return;
     float res[PER];
 #pragma unroll
@@ -258,12 +280,26 @@ __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs
             float den = 0.f, num[PER];
 #pragma unroll
             for (int j = 0; j < PER; ++j) num[j] = 0.f;
-            for (int q = 0; q < np; ++q) {
-                const float w = fast_exp2(lse[q] - M);
-                den += w;
-                const float *v = po + (size_t)q * D;
+            for (int q0 = 0; q0 < np; q0 += 32) {
+                // lane q holds the weight of part q0 + q
+                const float wq = q0 + lane < np ? fast_exp2(lse[q0 + lane] - M) : 0.f;
+                const int nq = np - q0 < 32 ? np - q0 : 32;
+#pragma unroll 4
+                for (int q = 0; q < nq; ++q) {
+                    const float w = __shfl_sync(0xffffffffu, wq, q);
+                    den += w;
+                    const float *v = po + (size_t)(q0 + q) * D;
+                    if constexpr (PER == 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(v);
+                        num[0] = fmaf(w, x.x, num[0]);
+                        num[1] = fmaf(w, x.y, num[1]);
+                        num[2] = fmaf(w, x.z, num[2]);
+                        num[3] = fmaf(w, x.w, num[3]);
+                    } else {
 #pragma unroll
-                for (int j = 0; j < PER; ++j) num[j] = fmaf(w, v[j], num[j]);
+                        for (int j = 0; j < PER; ++j) num[j] = fmaf(w, v[j], num[j]);
+                    }
+                }
             }
 #pragma unroll
             for (int j = 0; j < PER; ++j) res[j] = den > 0.f ? num[j] / den : 0.f;
@@ -348,6 +384,7 @@ extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
     p.dev_error = pool->dev_error;
     p.entries = reinterpret_cast<SpEntry *>(ws + lay.entries);
     p.nparts = reinterpret_cast<int32_t *>(ws + lay.nparts);
+    p.share = reinterpret_cast<int32_t *>(ws + lay.share);
     p.header = reinterpret_cast<int32_t *>(ws + lay.header);
     p.num_groups = num_groups;
     p.num_seqs = num_seqs;
@@ -357,7 +394,8 @@ extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
     p.pbp = z.ptp > 0 ? z.ptp / BS : ((maxp + BS - 1) / BS > 0 ? (maxp + BS - 1) / BS : 1);
     p.pbs = z.pts > 0 ? z.pts / BS : (cap_blocks > 0 ? cap_blocks : 1);
     p.members_per_item = kSpRowsMax / group;
-    p.max_entries = (int)max_entries;
+    p.prefix_cap = num_seqs * z.pp;
+    p.suffix_cap = num_seqs * z.ps;
     shared_prefix_plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
     if (cuda_status(cudaGetLastError()) != PKV_OK) return PKV_ERR_CUDA;
 
@@ -371,8 +409,11 @@ extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
     a.dev_error = pool->dev_error;
     a.entries = p.entries;
     a.nparts = p.nparts;
-    a.counter = p.header + 1;
+    a.seq_share = p.share;
+    a.block_tables_chk = block_tables;
+    a.counter = p.header + 2;
     a.count = p.header;
+    a.suffix_base = p.prefix_cap;
     a.num_heads = num_heads;
     a.num_kv_heads = num_kv_heads;
     a.group = group;
@@ -396,10 +437,17 @@ extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
         pool->head_dim == 64 ? launch_shared_prefix_d64(L) : launch_shared_prefix_d128(L);
     if (s1 != PKV_OK) return s1;
 
-    const unsigned nb = (unsigned)(((long long)num_seqs * num_heads + 7) / 8);
+    // the combine waits for the decode grid in griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(((long long)num_seqs * num_heads + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (pool->head_dim == 64)
-        shared_prefix_combine_kernel<64><<<nb, 256, 0, st>>>(a, num_seqs);
-    else
-        shared_prefix_combine_kernel<128><<<nb, 256, 0, st>>>(a, num_seqs);
-    return cuda_status(cudaGetLastError());
+        return cuda_status(cudaLaunchKernelEx(&cfg, shared_prefix_combine_kernel<64>, a, num_seqs));
+    return cuda_status(cudaLaunchKernelEx(&cfg, shared_prefix_combine_kernel<128>, a, num_seqs));
 }

@@ -11,11 +11,16 @@
 // the query rows of every member (members x GQA group <= 32 rows, two 16-row
 // mma.sync tiles), while "suffix items" walk each sequence's own blocks.
 // Every item leaves a normalised partial output and its log2-sum-exp per
-// query row; the combine pass merges them, which is exact for softmax.
+// query row (or the final row when it is the sequence's only part); the
+// combine pass merges the parts, which is exact for softmax.
 //
-// Work is a list written by a planning kernel and pulled by a persistent grid
-// (one atomic counter), prefix items first, so CTAs stay busy to the end and
-// no CTA is launched for an empty partition.
+// Work is a list written by the planning kernel and pulled, one item per
+// warp, from an atomic counter by a persistent grid: prefix items first (the
+// largest), then suffix items.  A warp runs its item alone, through its own
+// ring of TMA stages, so no warp ever waits for another: when its last block
+// is in it already stages the first blocks of its next item (whose entry,
+// block ids and partial counts it fetched while the current item streamed),
+// then writes its rows straight from registers.
 #pragma once
 
 #include <math_constants.h>
@@ -25,36 +30,44 @@
 namespace pkv {
 
 constexpr int kSpWarps = 4;
-#ifndef PKV_SP_STAGE_BUDGET
-#define PKV_SP_STAGE_BUDGET 98304
-#endif
+// Shared memory per CTA: two CTAs (8 warps) per SM, which is what the
+// register budget of the two-tile accumulators allows.
+constexpr int kSpSmemTarget = 112 * 1024;
 
-template <int D, int BS>
-constexpr int sp_stages() {
-    constexpr int per = kSpWarps * Geom<__nv_bfloat16, D, BS>::kStageBytes;
-    constexpr int n = PKV_SP_STAGE_BUDGET / per;
-    return n < 2 ? 2 : (n > 8 ? 8 : n);
-}
-
-// Per-warp state exported for the cross-warp merge.
-template <int D>
-struct SpState {
-    float m[kSpRowsMax];
-    float l[kSpRowsMax];
-    float o[kSpRowsMax][D];
-};
-
-// Shared memory: [ring | warp states] (aliased: the states are written only
-// once the ring is idle), the query tile, the mbarriers, the item header.
 template <int D, int BS>
 struct SpSmem {
-    static constexpr int kRing = kSpWarps * sp_stages<D, BS>() * Geom<__nv_bfloat16, D, BS>::kStageBytes;
-    static constexpr int kStates = kSpWarps * (int)sizeof(SpState<D>);
-    static constexpr int kRegion = ((kRing > kStates ? kRing : kStates) + 1023) / 1024 * 1024;
-    static constexpr int kQ = kSpRowsMax * D * 2;  // bf16 rows, 128-byte slabs, swizzled
-    static constexpr int kBars = kSpWarps * sp_stages<D, BS>() * 8;
+    using Gm = Geom<__nv_bfloat16, D, BS>;
+    static constexpr int kQ = kSpRowsMax * D * 2;  // a warp's query rows (bf16, swizzled slabs)
     static constexpr int kMisc = 256;
-    static constexpr int kBytes = kRegion + kQ + kBars + kMisc + 1024;
+    static constexpr int kFixed = kSpWarps * kQ + kMisc + 1024;
+    static constexpr int kStagesFit = (kSpSmemTarget - kFixed) / (kSpWarps * Gm::kStageBytes);
+    static constexpr int NST = kStagesFit < 2 ? 2 : (kStagesFit > 8 ? 8 : kStagesFit);
+    static constexpr int kRing = kSpWarps * NST * Gm::kStageBytes;
+    static constexpr int kBars = kSpWarps * NST * 8;
+    // offsets from the 1024-aligned base
+    static constexpr int oQ = kRing;
+    static constexpr int oBars = oQ + kSpWarps * kQ;
+    static constexpr int kBytes = oBars + kBars + kMisc + 1024;
+};
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte asynchronous global->shared copy; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// A work item as its warp sees it (fields of SpEntry plus derived values).
+struct SpItem {
+    int g, seq0, nseq, tbl_seq, b0, b1, slot, tok_end;
+    int nb;  // blocks of the item
+    int R;   // query rows (nseq * group)
 };
 
 // ------------------------------------------------------ tensor-core rows
@@ -85,7 +98,7 @@ struct SpMma {
 
     // Tokens r0 .. r0+15 of the staged block (K at kaddr, V at vaddr), the
     // first `nvalid` (1..16) of which are context tokens; query tile at qaddr.
-    template <int MT>
+    template <int MT, int QR>
     __device__ __forceinline__ void sub_block(uint32_t kaddr, uint32_t vaddr, uint32_t qaddr,
                                               int r0, int nvalid, float scale_log2, int lane) {
         float s[MT][2][4];
@@ -102,7 +115,7 @@ struct SpMma {
                 const int qrow = t * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    ldsm_x4(qaddr + swz_offset<kSpRowsMax>(qrow, (2 * kc + h) * 2 + (lane >> 4)),
+                    ldsm_x4(qaddr + swz_offset<QR>(qrow, (2 * kc + h) * 2 + (lane >> 4)),
                             qa[t][h][0], qa[t][h][1], qa[t][h][2], qa[t][h][3]);
             }
 #pragma unroll
@@ -199,38 +212,14 @@ struct SpMma {
         }
     }
 
-    template <int MT>
+    // query buffer of QR rows (32: two tiles for a prefix item; 16: one warp's own)
+    template <int MT, int QR>
     __device__ __forceinline__ void block(uint32_t kaddr, uint32_t vaddr, uint32_t qaddr, int nvalid,
                                           float scale_log2, int lane) {
 #pragma unroll
         for (int h = 0; h < BS / 16; ++h) {
             const int nv = nvalid - h * 16;
-            if (nv > 0) sub_block<MT>(kaddr, vaddr, qaddr, h * 16, nv < 16 ? nv : 16, scale_log2, lane);
-        }
-    }
-
-    template <int MT>
-    __device__ __forceinline__ void finish(SpState<D> *st) {
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            float l0 = l[t][0], l1 = l[t][1];
-            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-            const int r = t * 16 + gid;
-#pragma unroll
-            for (int n = 0; n < ND; ++n) {
-                const int d = n * 8 + 2 * tig;
-                *reinterpret_cast<float2 *>(&st->o[r][d]) = make_float2(o[t][n][0], o[t][n][1]);
-                *reinterpret_cast<float2 *>(&st->o[r + 8][d]) = make_float2(o[t][n][2], o[t][n][3]);
-            }
-            if (tig == 0) {
-                st->m[r] = m[t][0];
-                st->l[r] = l0;
-                st->m[r + 8] = m[t][1];
-                st->l[r + 8] = l1;
-            }
+            if (nv > 0) sub_block<MT, QR>(kaddr, vaddr, qaddr, h * 16, nv < 16 ? nv : 16, scale_log2, lane);
         }
     }
 };
@@ -243,198 +232,230 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                                 const __grid_constant__ CUtensorMap tmv, const SpArgs a) {
     using Gm = Geom<__nv_bfloat16, D, BS>;
     using Sm = SpSmem<D, BS>;
-    constexpr int NW = kSpWarps;
-    constexpr int NST = sp_stages<D, BS>();
+    constexpr int NST = Sm::NST;
     constexpr int QCH = D * 2 / 16;  // 16-byte chunks per query row
+    constexpr int ND = D / 8;
+    constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char *qtile = smem + Sm::kRegion;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(qtile + Sm::kQ);
-    int *misc = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(bars) + Sm::kBars);
-    int *s_next = misc;          // next item index
-    int *s_np = misc + 32;       // partial count of each row's sequence
-    SpState<D> *states = reinterpret_cast<SpState<D> *>(smem);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = a.num_kv_heads, G = a.group;
     unsigned char *wstage = smem + warp * NST * Gm::kStageBytes;
-    uint64_t *wbar = bars + warp * NST;
+    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + Sm::oBars) + warp * NST;
+    const uint32_t qaddr = smem_u32(smem + Sm::oQ + warp * Sm::kQ);
     if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < NST; ++i) mbar_init(&wbar[i], 1);
         fence_mbar_init();
-        if (warp == 0) {
-            tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
-        }
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
     }
-    if (threadIdx.x == 0) *s_next = atomicAdd(a.counter, 1);
-    __syncthreads();
-    const int total = __ldg(a.count) * Hkv;
+    __syncwarp();
+    griddep_wait();  // the work list of the planning kernel is complete and visible
+    const int nP = a.count[0], nS = a.count[1];
+    const int totalP = nP * Hkv, total = (nP + nS) * Hkv;
+
+    auto fetch = [&]() -> int {
+        int v = 0;
+        if (lane == 0) v = atomicAdd(a.counter, 1);
+        return __shfl_sync(FULL, v, 0);
+    };
+    // lane j < 8 holds field j of an item's entry (prefix items, then suffix items)
+    auto field = [&](int j) -> int {
+        if (j >= total) return 0;
+        const int e = j < totalP ? j / Hkv : a.suffix_base + (j - totalP) / Hkv;
+        return lane < 8 ? reinterpret_cast<const int *>(a.entries + e)[lane] : 0;
+    };
+    auto decode = [&](int j, int f) -> SpItem {
+        SpItem t;
+        t.g = (j < totalP ? j : j - totalP) % Hkv;
+        t.seq0 = __shfl_sync(FULL, f, 0);
+        t.nseq = __shfl_sync(FULL, f, 1);
+        t.tbl_seq = __shfl_sync(FULL, f, 2);
+        t.b0 = __shfl_sync(FULL, f, 3);
+        t.b1 = __shfl_sync(FULL, f, 4);
+        t.slot = __shfl_sync(FULL, f, 5);
+        t.tok_end = __shfl_sync(FULL, f, 6);
+        t.nb = t.b1 - t.b0;
+        t.R = t.nseq * G;
+        return t;
+    };
+    // physical block of the item's i-th block (chunk of 32, one per lane)
+    auto bt_load = [&](const SpItem &t, int chunk) -> int {
+        const int i = chunk * 32 + lane;
+        if (i >= t.nb) return -1;
+        return __ldg(a.block_tables + (size_t)t.tbl_seq * a.max_blocks_per_seq + t.b0 + i);
+    };
+    // partial count of the sequence of row `lane` of the item
+    auto nparts_of = [&](const SpItem &t) -> int {
+        return lane < t.R ? a.nparts[t.seq0 + lane / G] : 0;
+    };
+    // stage the item's block at absolute ring position k
+    auto issue = [&](int g, unsigned k, int pb) {
+        if (lane == 0) {
+            uint64_t *bar = &wbar[k % NST];
+            if (pb >= 0 && pb < a.num_blocks) {
+                mbar_arrive_expect_tx(bar, Gm::kStageBytes);
+                unsigned char *dk = wstage + (k % NST) * Gm::kStageBytes;
+                unsigned char *dv = dk + Gm::kTileBytes;
+                const int y = (pb * Hkv + g) * BS;
+#pragma unroll
+                for (int sl = 0; sl < Gm::kSlabs; ++sl) {
+                    tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);
+                    tma_load_2d(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar);
+                }
+            } else {
+                raise_fault(a.dev_error, PKV_FAULT_BLOCK_ID);
+                mbar_arrive(bar);
+            }
+        }
+    };
+    // the item's query rows into the warp's buffer (zero rows pad the last tile)
+    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+    auto load_rows = [&](const SpItem &t) {
+        const int rows_pad = t.R > 16 ? 32 : 16;
+#pragma unroll 2
+        for (int idx = lane; idx < rows_pad * QCH; idx += 32) {
+            const int r = idx / QCH, c = idx - r * QCH;
+            const __nv_bfloat16 *src = qg;
+            int bytes = 0;
+            if (r < t.R) {
+                const int sq = t.seq0 + r / G, h = t.g * G + r % G;
+                src = qg + ((size_t)sq * a.num_heads + h) * D + c * 8;
+                bytes = 16;
+            }
+            cp_async16(qaddr + swz_offset<kSpRowsMax>(r, c), src, bytes);
+        }
+        cp_async_commit();
+    };
 
     SpMma<D, BS> path;
     unsigned ctr = 0;  // blocks this warp has consumed (stage ring position, across items)
-    bool alive = true;
+    int j0 = fetch();
+    if (j0 < total) {
+        int j1 = fetch();
+        SpItem it = decode(j0, field(j0));
+        int f1 = field(j1);
+        load_rows(it);
+        int np = nparts_of(it);
+        int ent0 = bt_load(it, 0), ent1 = bt_load(it, 1);
 #pragma unroll 1
-    for (;;) {
-        const int item = *s_next;
-        if (item >= total) break;
-        __syncthreads();  // every thread has read s_next; the previous item's merge is done
-        if (threadIdx.x == 0) *s_next = atomicAdd(a.counter, 1);
-        const int e = item / Hkv, g = item - e * Hkv;
-        const SpEntry en = a.entries[e];
-        const int R = en.nseq * G;
-        const bool two = R > 16;
-        const int32_t *bt_row = a.block_tables + (size_t)en.tbl_seq * a.max_blocks_per_seq;
-
-        // this warp's logical blocks: en.b0 + warp + i*NW, i < nw
-        const int span = en.b1 - en.b0;
-        const int nw = span > warp ? (span - warp + NW - 1) / NW : 0;
-        auto bt_load = [&](int chunk) -> int {
-            const int i = chunk * 32 + lane;
-            if (i >= nw) return -1;
-            const int blk = en.b0 + warp + i * NW;
-            const int pb = __ldg(bt_row + blk);
-            if (en.check) {  // members must name the same physical block
-                bool bad = false;
-                for (int m = 0; m < en.nseq; ++m) {
-                    const int sq = en.seq0 + m;
-                    if (sq != en.tbl_seq &&
-                        __ldg(a.block_tables + (size_t)sq * a.max_blocks_per_seq + blk) != pb)
-                        bad = true;
-                }
-                if (bad) raise_fault(a.dev_error, PKV_FAULT_PREFIX);
+        for (int j = 0; j < NST && j < it.nb; ++j) issue(it.g, j, __shfl_sync(FULL, ent0, j));
+#pragma unroll 1
+        for (;;) {
+            cp_async_wait_all();
+            __syncwarp();  // the item's query rows are in place
+            // the item after next: index and entry; the next one: block ids and partial counts
+            const bool has_next = j1 < total;
+            const int j2 = fetch();
+            const int f2 = field(j2);
+            int entn0 = -1, entn1 = -1, np1 = 0;
+            if (has_next) {
+                const SpItem n1 = decode(j1, f1);
+                entn0 = bt_load(n1, 0);
+                entn1 = bt_load(n1, 1);
+                np1 = nparts_of(n1);
             }
-            return pb;
-        };
-        int ent0 = bt_load(0), ent1 = bt_load(1);
-        int cb = 0;
-        auto bt_get = [&](int i) -> int {
-            const int v0 = __shfl_sync(0xffffffffu, ent0, i & 31);
-            const int v1 = __shfl_sync(0xffffffffu, ent1, i & 31);
-            return (i >> 5) == cb ? v0 : v1;
-        };
-        auto issue = [&](int i, int pb) {
-            if (lane == 0) {
-                const unsigned k = ctr + i;
-                uint64_t *bar = &wbar[k % NST];
+            const bool two = it.R > 16;
+            path.reset(lane);
+            int cb = 0;
+            bool ok = true;
+            auto bt_get = [&](int i) -> int {
+                return (i >> 5) == cb ? __shfl_sync(FULL, ent0, i & 31) : __shfl_sync(FULL, ent1, i & 31);
+            };
+            int i = 0;
+#pragma unroll 1
+            for (; i < it.nb; ++i) {
+                if ((i >> 5) != cb) {
+                    cb = i >> 5;
+                    ent0 = ent1;
+                    ent1 = bt_load(it, cb + 1);
+                }
+                const int pb = bt_get(i);
+                const unsigned kk = ctr + i;
+                ok = __all_sync(FULL, mbar_wait(&wbar[kk % NST], (kk / NST) & 1));
+                if (!ok) break;
                 if (pb >= 0 && pb < a.num_blocks) {
-                    mbar_arrive_expect_tx(bar, Gm::kStageBytes);
-                    unsigned char *dk = wstage + (k % NST) * Gm::kStageBytes;
-                    unsigned char *dv = dk + Gm::kTileBytes;
-                    const int y = (pb * Hkv + g) * BS;
+                    const int nvalid = min(BS, it.tok_end - (it.b0 + i) * BS);
+                    const uint32_t kaddr = smem_u32(wstage + (kk % NST) * Gm::kStageBytes);
+                    if (two)
+                        path.template block<2, kSpRowsMax>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
+                                                           a.scale_log2, lane);
+                    else
+                        path.template block<1, kSpRowsMax>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
+                                                           a.scale_log2, lane);
+                }
+                __syncwarp();
+                if (i + NST < it.nb) issue(it.g, kk + NST, bt_get(i + NST));
+            }
+            if (!ok) {
+                if (lane == 0) raise_fault(a.dev_error, PKV_FAULT_TIMEOUT);
+                // drain what this warp still has in flight, again with a bound
+                for (int j = i; j < it.nb && j < i + NST; ++j) {
+                    const unsigned kk = ctr + j;
+                    mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
+                }
+                break;
+            }
+            ctr += it.nb;
+            SpItem nx = it;
+            if (has_next) {
+                // the next item's first stages and query rows, before this item's epilogue
+                nx = decode(j1, f1);
+#pragma unroll 1
+                for (int j = 0; j < NST && j < nx.nb; ++j) issue(nx.g, ctr + j, __shfl_sync(FULL, entn0, j));
+                load_rows(nx);  // every lane is past its last ldmatrix of the buffer
+            }
+            // epilogue: rows gid and gid+8 of each tile, straight from registers
+            const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
-                    for (int sl = 0; sl < Gm::kSlabs; ++sl) {
-                        tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);
-                        tma_load_2d(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar);
+            for (int t = 0; t < 2; ++t) {
+                if (t == 1 && !two) break;
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    float L = path.l[t][hr];
+                    L += __shfl_xor_sync(FULL, L, 1);
+                    L += __shfl_xor_sync(FULL, L, 2);
+                    const int r = t * 16 + gid + hr * 8;
+                    const int npr = __shfl_sync(FULL, np, r);
+                    if (r < it.R) {
+                        const float invL = L > 0.f ? 1.f / L : 0.f;
+                        const size_t sh = (size_t)(it.seq0 + r / G) * a.num_heads + it.g * G + r % G;
+#pragma unroll
+                        for (int n = 0; n < ND; ++n) {
+                            const int d = n * 8 + 2 * tig;
+                            const float2 v = make_float2(path.o[t][n][2 * hr] * invL,
+                                                         path.o[t][n][2 * hr + 1] * invL);
+                            if (npr == 1) {
+                                if (a.out_bf16)
+                                    *reinterpret_cast<uint32_t *>(
+                                        reinterpret_cast<__nv_bfloat16 *>(a.out) + sh * D + d) =
+                                        pack_bf16(v.x, v.y);
+                                else
+                                    *reinterpret_cast<float2 *>(reinterpret_cast<float *>(a.out) +
+                                                                sh * D + d) = v;
+                            } else {
+                                const size_t pi = sh * a.num_slots + it.slot;
+                                *reinterpret_cast<float2 *>(a.ws_o + pi * D + d) = v;
+                                if (n == 0 && tig == 0)
+                                    a.ws_lse[pi] = L > 0.f ? path.m[t][hr] + __log2f(L) : -CUDART_INF_F;
+                            }
+                        }
                     }
-                } else {
-                    raise_fault(a.dev_error, PKV_FAULT_BLOCK_ID);
-                    mbar_arrive(bar);
                 }
             }
-        };
-#pragma unroll 1
-        for (int i = 0; i < NST && i < nw; ++i) issue(i, bt_get(i));
-
-        // query rows of the item (zero rows pad the last 16-row tile)
-        const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-        const int rows_pad = two ? 32 : 16;
-#pragma unroll 1
-        for (int idx = threadIdx.x; idx < rows_pad * QCH; idx += NW * 32) {
-            const int r = idx / QCH, c = idx - r * QCH;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < R) {
-                const int sq = en.seq0 + r / G, h = g * G + r % G;
-                v = __ldg(reinterpret_cast<const uint4 *>(q + ((size_t)sq * a.num_heads + h) * D) + c);
-            }
-            *reinterpret_cast<uint4 *>(qtile + swz_offset<kSpRowsMax>(r, c)) = v;
+            if (!has_next) break;
+            it = nx;
+            j1 = j2;
+            f1 = f2;
+            np = np1;
+            ent0 = entn0;
+            ent1 = entn1;
         }
-        if (threadIdx.x < R) s_np[threadIdx.x] = __ldg(a.nparts + en.seq0 + threadIdx.x / G);
-        __syncthreads();
-
-        path.reset(lane);
-        const uint32_t qaddr = smem_u32(qtile);
-        int i = 0;
-        bool ok = true;
-#pragma unroll 1
-        for (; i < nw; ++i) {
-            if ((i >> 5) != cb) {
-                cb = i >> 5;
-                ent0 = ent1;
-                ent1 = bt_load(cb + 1);
-            }
-            const int pb = bt_get(i);
-            const unsigned k = ctr + i;
-            ok = __all_sync(0xffffffffu, mbar_wait(&wbar[k % NST], (k / NST) & 1));
-            if (!ok) break;
-            if (pb >= 0 && pb < a.num_blocks) {
-                const int lblk = en.b0 + warp + i * NW;
-                const int nvalid = min(BS, en.tok_end - lblk * BS);
-                const uint32_t kaddr = smem_u32(wstage + (k % NST) * Gm::kStageBytes);
-                if (two)
-                    path.template block<2>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid, a.scale_log2, lane);
-                else
-                    path.template block<1>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid, a.scale_log2, lane);
-            }
-            __syncwarp();
-            if (i + NST < nw) issue(i + NST, bt_get(i + NST));
-        }
-        if (!ok) {
-            if (lane == 0) raise_fault(a.dev_error, PKV_FAULT_TIMEOUT);
-            // drain what this warp still has in flight, again with a bound
-            for (int j = i; j < nw && j < i + NST; ++j) {
-                const unsigned k = ctr + j;
-                mbar_wait(&wbar[k % NST], (k / NST) & 1);
-            }
-            alive = false;
-        }
-        ctr += nw;
-
-        // ---- merge the warps' states in the (now idle) ring
-        __syncthreads();
-        if (two)
-            path.template finish<2>(&states[warp]);
-        else
-            path.template finish<1>(&states[warp]);
-        __syncthreads();
-#pragma unroll 1
-        for (int idx = threadIdx.x; idx < R * D; idx += NW * 32) {
-            const int r = idx / D, d = idx - r * D;
-            float M = -CUDART_INF_F;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, states[w].m[r]);
-            float L = 0.f, O = 0.f;
-            if (M != -CUDART_INF_F) {
-#pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const float f = fast_exp2(states[w].m[r] - M);
-                    L += states[w].l[r] * f;
-                    O += states[w].o[r][d] * f;
-                }
-            }
-            const float res = L > 0.f ? O / L : 0.f;
-            const int sq = en.seq0 + r / G, h = g * G + r % G;
-            const size_t sh = (size_t)sq * a.num_heads + h;
-            if (s_np[r] == 1) {
-                if (a.out_bf16)
-                    reinterpret_cast<__nv_bfloat16 *>(a.out)[sh * D + d] = __float2bfloat16_rn(res);
-                else
-                    reinterpret_cast<float *>(a.out)[sh * D + d] = res;
-            } else {
-                const size_t pi = sh * a.num_slots + en.slot;
-                a.ws_o[pi * D + d] = res;
-                if (d == 0) a.ws_lse[pi] = L > 0.f ? M + __log2f(L) : -CUDART_INF_F;
-            }
-        }
-        // the next item's TMA copies overwrite the states: order this thread's
-        // generic shared-memory accesses before them
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        // a warp that gave up leaves the CTA's loop once the merge is done
-        if (__syncthreads_or(!alive)) break;
     }
+    griddep_launch();
 }
 
 template <int D, int BS>
@@ -457,8 +478,19 @@ pkv_status launch_sp_one(const SpLaunch &L) {
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
     }
     const int grid = __atomic_load_n(&per_sm[L.device & 63], __ATOMIC_RELAXED) * sm_count(L.device);
-    kern<<<grid, kSpWarps * 32, smem, L.stream>>>(*L.tmk, *L.tmv, L.args);
-    return cuda_status(cudaGetLastError());
+    // launched as a programmatic dependent of the planning kernel: the CTAs
+    // set up while the plan finishes and wait for it in griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kSpWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, *L.tmk, *L.tmv, L.args));
 }
 
 template <int D>
