@@ -44,6 +44,8 @@ NCU_TRAFFIC: dict = {
     # profiles/paged_decode_kernel_mha_7b_gqa_8b.md
     ("mha_7b", "plain"): {"bytes": 1105897000 + 5756160, "src": "2c19345f8540f6ba"},
     ("gqa_8b", "plain"): {"bytes": 2374157000 + 13745152, "src": "2c19345f8540f6ba"},
+    # profiles/shared_prefix_decode_kernel_shared_prefix.md
+    ("shared_prefix", "shared"): {"bytes": 856210944 + 40355584, "src": "33cf1116db80e0d1"},
 }
 
 

@@ -152,3 +152,61 @@ def test_block_table_upload_checks_entries_on_host(lib):
     assert up(0, host.ctypes.data, 2, 3, 0, None) == pagedkv.ERR_INVALID_ARG
     assert up(0x1000, host.ctypes.data, 2, 0, 0, None) == pagedkv.ERR_INVALID_ARG
     assert up(0x1000, host.ctypes.data, 0, 3, 0, None) == pagedkv.OK
+
+
+def _sp_decode(lib, pool, **kw):
+    args = dict(out=0x1000, out_dtype=pagedkv.F32, query=0x2000, num_seqs=4, num_heads=8,
+                num_kv_heads=2, block_tables=0x3000, max_blocks=8, context_lens=0x4000,
+                max_ctx=128, scale=0.1, group_starts=0x5000, prefix_lens=0x6000, num_groups=2,
+                max_prefix=64, partition=0, ws=0x7000, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.pkv_paged_attention_decode_shared_prefix(
+        ctypes.byref(pool) if pool is not None else None, args["out"], args["out_dtype"],
+        args["query"], args["num_seqs"], args["num_heads"], args["num_kv_heads"],
+        args["block_tables"], args["max_blocks"], args["context_lens"], args["max_ctx"],
+        args["scale"], args["group_starts"], args["prefix_lens"], args["num_groups"],
+        args["max_prefix"], args["partition"], args["ws"], args["ws_bytes"], args["stream"])
+
+
+def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib):
+    E, U = pagedkv.ERR_INVALID_ARG, pagedkv.ERR_UNSUPPORTED
+    pool = _fake_pool()
+    assert _sp_decode(lib, None) == E                                # no pool
+    assert _sp_decode(lib, pagedkv.pkv_pool()) == E                  # not initialised
+    assert _sp_decode(lib, pool, num_groups=0) == E                  # groups must cover the batch
+    assert _sp_decode(lib, pool, num_groups=5) == E                  # more groups than sequences
+    assert _sp_decode(lib, pool, group_starts=0) == E
+    assert _sp_decode(lib, pool, prefix_lens=0x6002) == E            # misaligned
+    assert _sp_decode(lib, pool, max_prefix=-1) == E
+    assert _sp_decode(lib, pool, partition=24) == E                  # not a block multiple
+    assert _sp_decode(lib, pool, num_kv_heads=4) == E                # != pool heads
+    assert _sp_decode(lib, pool, scale=float("inf")) == E
+    assert _sp_decode(lib, _fake_pool(dtype=pagedkv.F32)) == U       # bf16 pools only
+    assert _sp_decode(lib, pool, num_heads=34) == U                  # group 17 > 16
+    assert _sp_decode(lib, pool, num_seqs=0) == pagedkv.OK           # nothing to do
+
+
+def test_shared_prefix_workspace_bytes(lib):
+    """Header, per-sequence counts and sharing records, the work list, and
+    the partials: one slot per prefix part (512-token parts by default) and
+    per own part (512 tokens) of the longest sequence."""
+    r = lambda x: -(-x // 256) * 256  # noqa: E731
+
+    def expect(S, H, D, maxc, maxp, pt):
+        mp = min(maxp, maxc)
+        if pt < 0:
+            pp, ps = int(mp > 0), int(maxc > 0)
+        else:
+            ptp = pts = pt if pt > 0 else 512
+            pp, ps = -(-mp // ptp), -(-maxc // pts)
+        slots = max(pp + ps, 1)
+        return (256 + r(S * 4) + r(S * 8) + r(S * slots * 32) + r(S * H * slots * 4) +
+                r(S * H * slots * D * 4))
+
+    f = lib.pkv_shared_prefix_workspace_bytes
+    for S, H, D, maxc, maxp, pt in [(256, 32, 128, 4608, 4096, 0), (8, 64, 128, 131072, 0, 0),
+                                    (3, 4, 64, 100, 48, 32), (5, 8, 128, 2000, 1024, -1),
+                                    (2, 2, 64, 64, 999, 0)]:
+        assert f(S, H, D, maxc, maxp, pt) == expect(S, H, D, maxc, maxp, pt), (S, maxc, maxp, pt)
+    assert f(0, 8, 128, 100, 0, 0) == 0
+    assert f(4, 8, 128, 100, -1, 0) == 0
