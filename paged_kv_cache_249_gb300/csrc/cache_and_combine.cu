@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256)
                              const int64_t *__restrict__ slot_mapping, int num_tokens,
                              int num_kv_heads, int block_size, int chunks_per_row,
                              long long num_slots, int32_t *dev_error) {
+    griddep_launch();  // a decode launched behind this kernel may start its set-up
     const long long per_token = (long long)num_kv_heads * chunks_per_row;
     const long long total = per_token * num_tokens;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -107,6 +108,7 @@ pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const in
 __global__ void __launch_bounds__(128)
     lse_combine_kernel(const DecodeArgs a, int head_dim, int block_size) {
     __shared__ float red[4];
+    griddep_wait();  // the decode grid's partials are complete
     const int sh = blockIdx.x;  // s * H + h
     const int s = sh / a.num_heads;
     int ctx = __ldg(a.context_lens + s);
@@ -147,8 +149,8 @@ pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, i
                               cudaStream_t stream) {
     const long long n = (long long)num_seqs * a.num_heads;
     if (n == 0) return PKV_OK;
-    lse_combine_kernel<<<(unsigned)n, 128, 0, stream>>>(a, head_dim, block_size);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_dependent(lse_combine_kernel, dim3((unsigned)n), dim3(128), 0, stream,
+                                        a, head_dim, block_size));
 }
 
 }  // namespace pkv

@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     const int s = blockIdx.x, g = blockIdx.y, part = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_wait();  // inputs written by the kernel before this one are complete
 
     // Gather this warp's first block numbers before the context length is
     // known (bounded by the table row), so the two dependent loads overlap.
@@ -605,6 +606,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             if (d == 0) a.ws_lse[pi] = L > 0.f ? M + __log2f(L) : -CUDART_INF_F;
         }
     }
+    griddep_launch();
 }
 
 // Explicit-instantiation helper: launch one configuration.
@@ -623,8 +625,8 @@ pkv_status launch_one(const DecodeLaunch &L) {
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
     }
     dim3 grid(L.num_seqs, L.args.num_kv_heads, L.args.num_parts);
-    kern<<<grid, kDecodeWarps * 32, smem, L.stream>>>(*L.tmk, *L.tmv, L.args);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(
+        launch_dependent(kern, grid, dim3(kDecodeWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }
 
 template <typename T, int D, int BS>

@@ -30,6 +30,36 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Wait until the grid this one was launched behind (as a programmatic
+// dependent) has completed and its writes are visible; a no-op otherwise.
+// Every read of a kernel input comes after it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid in the stream, if launched as a programmatic dependent,
+// start its set-up now (it still waits in griddep_wait for this grid to end).
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kern` as a programmatic dependent of the previous kernel in
+// `stream`: its CTAs may be scheduled while that kernel finishes.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {

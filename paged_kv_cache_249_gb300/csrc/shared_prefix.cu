@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     __shared__ int s_ctx[kPlanSmemSeqs];
     // the decode kernel may start setting up; it waits for this grid in
     // griddepcontrol.wait before it reads anything written here
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    griddep_launch();
     const int tid = threadIdx.x;
     const bool staged = p.num_seqs <= kPlanSmemSeqs;
     bool bad = false;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
 template <int D>
 __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs a, int num_seqs) {
     constexpr int PER = D / 32;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    griddep_wait();
     const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (wid >= num_seqs * a.num_heads) return;
     const int s = wid / a.num_heads;
@@ -438,16 +438,10 @@ extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
     if (s1 != PKV_OK) return s1;
 
     // the combine waits for the decode grid in griddepcontrol.wait
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(((long long)num_seqs * num_heads + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 cgrid((unsigned)(((long long)num_seqs * num_heads + 7) / 8));
     if (pool->head_dim == 64)
-        return cuda_status(cudaLaunchKernelEx(&cfg, shared_prefix_combine_kernel<64>, a, num_seqs));
-    return cuda_status(cudaLaunchKernelEx(&cfg, shared_prefix_combine_kernel<128>, a, num_seqs));
+        return cuda_status(
+            launch_dependent(shared_prefix_combine_kernel<64>, cgrid, dim3(256), 0, st, a, num_seqs));
+    return cuda_status(
+        launch_dependent(shared_prefix_combine_kernel<128>, cgrid, dim3(256), 0, st, a, num_seqs));
 }

@@ -50,10 +50,6 @@ struct SpSmem {
     static constexpr int kBytes = oBars + kBars + kMisc + 1024;
 };
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // 16-byte asynchronous global->shared copy; src_bytes 0 writes zeros.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
@@ -480,17 +476,8 @@ pkv_status launch_sp_one(const SpLaunch &L) {
     const int grid = __atomic_load_n(&per_sm[L.device & 63], __ATOMIC_RELAXED) * sm_count(L.device);
     // launched as a programmatic dependent of the planning kernel: the CTAs
     // set up while the plan finishes and wait for it in griddepcontrol.wait
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kSpWarps * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, kern, *L.tmk, *L.tmv, L.args));
+    return cuda_status(
+        launch_dependent(kern, dim3(grid), dim3(kSpWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }
 
 template <int D>
