@@ -42,8 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 # sources hash to `src`.  Filled in from the profiles summaries.
 NCU_TRAFFIC: dict = {
     # profiles/paged_decode_kernel_mha_7b_gqa_8b.md
-    ("mha_7b", "plain"): {"bytes": 1105898000 + 5509888, "src": "5f9674d1ffe8bab6"},
-    ("gqa_8b", "plain"): {"bytes": 2374323000 + 13362432, "src": "5f9674d1ffe8bab6"},
+    ("mha_7b", "plain"): {"bytes": 1105898000 + 5509888, "src": "e8c95f027e4ecfd6"},
+    ("gqa_8b", "plain"): {"bytes": 2374323000 + 13362432, "src": "e8c95f027e4ecfd6"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md
     ("shared_prefix", "shared"): {"bytes": 856210944 + 40355584, "src": "33cf1116db80e0d1"},
 }
@@ -53,7 +53,7 @@ NCU_TRAFFIC: dict = {
 # recorded DRAM traffic stale).
 KERNEL_SOURCES = {
     "plain": ["decode_kernel.cuh", "pkv_device.cuh", "decode_bf16_d128.cu", "decode_bf16_d64.cu",
-              "decode_f32_d128.cu", "decode_f32_d64.cu", "cache_and_combine.cu"],
+              "decode_f32_d128.cu", "decode_f32_d64.cu"],
     "shared": ["shared_prefix_kernel.cuh", "shared_prefix.cu", "shared_prefix_d128.cu",
                "decode_kernel.cuh", "pkv_device.cuh"],
 }

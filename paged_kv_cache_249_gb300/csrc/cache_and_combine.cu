@@ -105,52 +105,132 @@ pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const in
 // partial outputs o_p and their log2-sum-exp lse_p.  The full softmax result
 // is sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M) with M = max_p lse_p,
 // which is exact: the partitions' exponentials share one max-free total.
-__global__ void __launch_bounds__(128)
-    lse_combine_kernel(const DecodeArgs a, int head_dim, int block_size) {
-    __shared__ float red[4];
-    griddep_wait();  // the decode grid's partials are complete
-    const int sh = blockIdx.x;  // s * H + h
-    const int s = sh / a.num_heads;
+// One CTA per (sequence, head); two kernels, chosen on the host by the
+// number of partitions of the longest allowed context.
+constexpr int kCombThreads = 128;
+constexpr int kCombChunk = 1024;
+constexpr int kCombDirect = 16;  // up to this many partitions, the direct loop is faster
+
+// Parts of (sequence, head) blockIdx.x: their count (0 or 1: nothing to do)
+// and the max of their log2-sum-exps over the CTA.
+struct CombRow {
+    int sh, nparts;
+    const float *lse, *po;
+};
+
+__device__ __forceinline__ CombRow comb_row(const DecodeArgs &a, int head_dim, int block_size) {
+    CombRow r;
+    r.sh = blockIdx.x;  // s * H + h
+    const int s = r.sh / a.num_heads;
     int ctx = __ldg(a.context_lens + s);
     ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
     const int nblk = (ctx + block_size - 1) / block_size;
-    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
-    if (nparts <= 1) return;  // the decode kernel wrote this row directly
-    const float *lse = a.ws_lse + (size_t)sh * a.num_parts;
-    const float *po = a.ws_o + (size_t)sh * a.num_parts * head_dim;
+    r.nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+    r.lse = a.ws_lse + (size_t)r.sh * a.num_parts;
+    r.po = a.ws_o + (size_t)r.sh * a.num_parts * head_dim;
+    return r;
+}
 
+__device__ __forceinline__ float comb_max(const CombRow &r, float *red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float M = -CUDART_INF_F;
-    for (int p = threadIdx.x; p < nparts; p += blockDim.x) M = fmaxf(M, lse[p]);
+    for (int p = tid; p < r.nparts; p += kCombThreads) M = fmaxf(M, r.lse[p]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
+    if (lane == 0) red[warp] = M;
     __syncthreads();
-    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombThreads / 32; ++w) M = fmaxf(M, red[w]);
+    return M;
+}
 
-    for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+__device__ __forceinline__ void comb_store(const DecodeArgs &a, size_t oi, float res) {
+    if (a.out_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(res);
+    else
+        reinterpret_cast<float *>(a.out)[oi] = res;
+}
+
+// Few partitions: each thread walks its column's parts directly.
+__global__ void __launch_bounds__(kCombThreads)
+    lse_combine_kernel(const DecodeArgs a, int head_dim, int block_size) {
+    __shared__ float red[kCombThreads / 32];
+    griddep_wait();  // the decode grid's partials are complete
+    const CombRow r = comb_row(a, head_dim, block_size);
+    if (r.nparts <= 1) return;  // the decode kernel wrote this row directly
+    const float M = comb_max(r, red);
+    for (int d = threadIdx.x; d < head_dim; d += kCombThreads) {
         float num = 0.f, den = 0.f;
         if (M != -CUDART_INF_F) {
-            for (int p = 0; p < nparts; ++p) {
-                const float w = fast_exp2(lse[p] - M);
+            for (int p = 0; p < r.nparts; ++p) {
+                const float w = fast_exp2(r.lse[p] - M);
                 den += w;
-                num = fmaf(w, po[(size_t)p * head_dim + d], num);
+                num = fmaf(w, r.po[(size_t)p * head_dim + d], num);
             }
         }
-        const float res = den > 0.f ? num / den : 0.f;
-        const size_t oi = (size_t)sh * head_dim + d;
-        if (a.out_bf16)
-            reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(res);
-        else
-            reinterpret_cast<float *>(a.out)[oi] = res;
+        comb_store(a, (size_t)r.sh * head_dim + d, den > 0.f ? num / den : 0.f);
     }
+}
+
+// Many partitions (a long context has hundreds): the weights 2^(lse_p - M)
+// are computed once into shared memory, kCombChunk parts at a time, and
+// every column is summed over the parts with eight independent loads in
+// flight per thread (head_dim 64: two threads per column, each every other
+// part).
+__global__ void __launch_bounds__(kCombThreads)
+    lse_combine_many_kernel(const DecodeArgs a, int head_dim, int block_size) {
+    __shared__ float w_s[kCombChunk];
+    __shared__ float red_m[kCombThreads / 32], red_d[kCombThreads / 32];
+    __shared__ float acc_s[kCombThreads];
+    griddep_wait();  // the decode grid's partials are complete
+    const CombRow r = comb_row(a, head_dim, block_size);
+    if (r.nparts <= 1) return;  // the decode kernel wrote this row directly
+    const float M = comb_max(r, red_m);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tpc = kCombThreads / head_dim;
+    const int d = tid % head_dim, pg = tid / head_dim;
+    float num = 0.f, den = 0.f;
+    for (int p0 = 0; p0 < r.nparts; p0 += kCombChunk) {
+        const int n = r.nparts - p0 < kCombChunk ? r.nparts - p0 : kCombChunk;
+        __syncthreads();  // the previous chunk's weights are consumed
+        for (int i = tid; i < n; i += kCombThreads) {
+            const float w = M == -CUDART_INF_F ? 0.f : fast_exp2(r.lse[p0 + i] - M);
+            w_s[i] = w;
+            den += w;
+        }
+        __syncthreads();
+        const float *col = r.po + (size_t)p0 * head_dim + d;
+        int i = pg;
+        for (; i + 7 * tpc < n; i += 8 * tpc) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = col[(size_t)(i + u * tpc) * head_dim];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) num = fmaf(w_s[i + u * tpc], v[u], num);
+        }
+        for (; i < n; i += tpc) num = fmaf(w_s[i], col[(size_t)i * head_dim], num);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if (lane == 0) red_d[warp] = den;
+    acc_s[tid] = num;
+    __syncthreads();
+    if (pg != 0) return;
+    den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombThreads / 32; ++w) den += red_d[w];
+    for (int q = 1; q < tpc; ++q) num += acc_s[d + q * head_dim];
+    comb_store(a, (size_t)r.sh * head_dim + d, den > 0.f ? num / den : 0.f);
 }
 
 pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, int block_size,
                               cudaStream_t stream) {
     const long long n = (long long)num_seqs * a.num_heads;
     if (n == 0) return PKV_OK;
-    return cuda_status(launch_dependent(lse_combine_kernel, dim3((unsigned)n), dim3(128), 0, stream,
-                                        a, head_dim, block_size));
+    auto kern = a.num_parts <= kCombDirect ? lse_combine_kernel : lse_combine_many_kernel;
+    return cuda_status(launch_dependent(kern, dim3((unsigned)n), dim3(kCombThreads), 0, stream, a,
+                                        head_dim, block_size));
 }
 
 }  // namespace pkv
