@@ -45,7 +45,7 @@ NCU_TRAFFIC: dict = {
     ("mha_7b", "plain"): {"bytes": 1105898000 + 5509888, "src": "e8c95f027e4ecfd6"},
     ("gqa_8b", "plain"): {"bytes": 2374323000 + 13362432, "src": "e8c95f027e4ecfd6"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md
-    ("shared_prefix", "shared"): {"bytes": 856210944 + 40355584, "src": "33cf1116db80e0d1"},
+    ("shared_prefix", "shared"): {"bytes": 856257024 + 40258048, "src": "174fcd69097c2fe0"},
 }
 
 
