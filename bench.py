@@ -351,9 +351,27 @@ def run_native(args, world: int, rank: int) -> dict | None:
         torch.cuda.synchronize()
         pl_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in pev])) * 1e3
         sp_us = float(np.mean(dec_ms)) * 1e3
+        # one plan serves every layer of a step: the decode and combine alone
+        dw.shared_prefix_plan()
+        for _ in range(args.warmup):
+            dw.decode_shared_prefix_run()
+        torch.cuda.synchronize()
+        rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a_, b_ in rev:
+            a_.record(stream)
+            dw.decode_shared_prefix_run()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        run_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in rev])) * 1e3
         plain_cmp = {"shared_prefix_decode_us": round(sp_us, 2), "plain_decode_us": round(pl_us, 2),
                      "plain_over_shared": round(pl_us / sp_us, 4),
-                     "max_abs_diff": float((dw.out.float() - ref_out.float()).abs().max())}
+                     "max_abs_diff": float((dw.out.float() - ref_out.float()).abs().max()),
+                     "per_layer_run_us": round(run_us, 2),
+                     "per_layer_run_frac": round(ab["decode_launch"] / (run_us * 1e-6) / 1e9 /
+                                                 measured_peak_gbs()[0], 4),
+                     "per_layer_note": "decode + combine from one plan (a step's layers share "
+                                       "its plan); the step above includes the plan"}
         decode()  # leave the shared-prefix output in dw.out
         torch.cuda.synchronize()
 

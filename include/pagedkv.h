@@ -264,8 +264,8 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * blocks are used), the offending group is then computed without sharing,
  * so the output is still exact.
  *
- * partition_tokens: 0 = automatic (prefix parts of 1024 tokens, per-sequence
- * parts of 512), -1 = one part each, > 0 = parts of that many tokens (a
+ * partition_tokens: 0 = automatic (parts of 512 tokens for the prefix and for
+ * each sequence's own blocks), -1 = one part each, > 0 = parts of that many tokens (a
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: bf16 pools,
@@ -280,6 +280,37 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
     const int32_t *context_lens, int max_context_len, float scale, const int32_t *group_starts,
     const int32_t *prefix_lens, int num_groups, int max_prefix_len, int partition_tokens,
     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The shared-prefix decode in two calls, for a model whose layers share one
+ * decode step's batch: the plan depends only on the group description and
+ * the context lengths, which every layer of a step has in common, so one
+ * plan serves all of them.
+ *
+ * pkv_shared_prefix_plan: checks the group description and writes the work
+ * list into `workspace` (arguments as in pkv_paged_attention_decode_shared_
+ * prefix; block tables and queries are not needed yet).
+ *
+ * pkv_paged_attention_decode_shared_prefix_run: the decode and combine from
+ * that plan, for one layer's pool, queries and output.  num_seqs, num_heads,
+ * num_kv_heads, the block size, max_context_len, max_prefix_len and
+ * partition_tokens must be those of the plan: a run whose geometry differs
+ * from the plan in the workspace (or that finds no plan there) sets
+ * PKV_FAULT_PREFIX and writes nothing.  Runs on one plan must be ordered on
+ * the GPU (one stream): each run's last kernel re-arms the plan for the
+ * next.  The block tables must be those the plan's groups describe.
+ */
+pkv_status pkv_shared_prefix_plan(const pkv_pool *pool, int num_seqs, int num_heads,
+                                  int num_kv_heads, int max_blocks_per_seq,
+                                  const int32_t *context_lens, int max_context_len,
+                                  const int32_t *group_starts, const int32_t *prefix_lens,
+                                  int num_groups, int max_prefix_len, int partition_tokens,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+pkv_status pkv_paged_attention_decode_shared_prefix_run(
+    const pkv_pool *pool, void *out, pkv_dtype out_dtype, const void *query, int num_seqs,
+    int num_heads, int num_kv_heads, const int32_t *block_tables, int max_blocks_per_seq,
+    int max_context_len, float scale, int max_prefix_len, int partition_tokens, void *workspace,
+    size_t workspace_bytes, void *stream);
 
 /*
  * Copy whole physical blocks (every kv head, K and V): block dst[i] becomes a

@@ -77,8 +77,11 @@ struct SpArgs {
     const int32_t *seq_share;   // [S][2] group leader and shared blocks (planning kernel)
     const int32_t *block_tables_chk;  // block tables, for the combine's agreement check
     int32_t *counter;           // work counter, zeroed by the planning kernel
-    const int32_t *count;       // [2]: prefix and suffix entries (planning kernel)
+    const int32_t *count;       // workspace header: [0], [1] prefix and suffix entries,
+                                // [kSpHdrMagic..] the plan's geometry (planning kernel)
     int suffix_base;
+    int num_seqs;
+    int block_size;
     int num_heads;
     int num_kv_heads;
     int group;
@@ -88,6 +91,19 @@ struct SpArgs {
     int out_bf16;
     float scale_log2;
 };
+
+// Workspace header of the shared-prefix plan: where the plan records the
+// geometry it was made for, and the value that marks a written plan.
+constexpr int kSpHdrMagic = 8;
+constexpr int32_t kSpPlanMagic = 0x50504c31;  // "PPL1"
+
+// Whether the plan in the workspace was made for this call's geometry.
+__host__ __device__ inline bool sp_plan_matches(const SpArgs &a) {
+    const int32_t *h = a.count + kSpHdrMagic;
+    return h[0] == kSpPlanMagic && h[1] == a.num_seqs && h[2] == a.num_heads &&
+           h[3] == a.num_kv_heads && h[4] == a.block_size && h[5] == a.num_slots &&
+           h[6] == a.suffix_base;
+}
 
 struct SpLaunch {
     const CUtensorMap *tmk;

@@ -82,6 +82,7 @@ struct SpPlan {
     int block_size;
     int pbp, pbs;           // blocks per prefix / suffix item
     int members_per_item;   // floor(32 / group)
+    int num_heads, num_kv_heads, slots;  // recorded in the header for the run's check
     int prefix_cap;         // entries [0, prefix_cap) hold prefix items
     int suffix_cap;         // entries [prefix_cap, prefix_cap + suffix_cap) hold suffix items
 };
@@ -236,7 +237,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     if (tid == 0) {
         p.header[0] = run_pre < p.prefix_cap ? run_pre : p.prefix_cap;
         p.header[1] = run_suf < p.suffix_cap ? run_suf : p.suffix_cap;
-        p.header[2] = 0;
+        p.header[2] = 0;  // work counter (the combine resets it after each run)
+        // the geometry this plan was made for; a run checks it
+        p.header[kSpHdrMagic] = kSpPlanMagic;
+        p.header[kSpHdrMagic + 1] = p.num_seqs;
+        p.header[kSpHdrMagic + 2] = p.num_heads;
+        p.header[kSpHdrMagic + 3] = p.num_kv_heads;
+        p.header[kSpHdrMagic + 4] = p.block_size;
+        p.header[kSpHdrMagic + 5] = p.slots;
+        p.header[kSpHdrMagic + 6] = p.prefix_cap;
     }
 }
 
@@ -250,6 +259,8 @@ template <int D>
 __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs a, int num_seqs) {
     constexpr int PER = D / 32;
     griddep_wait();
+    if (!sp_plan_matches(a)) return;  // the decode kernel reported it
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.counter = 0;  // ready for the next run
     const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (wid >= num_seqs * a.num_heads) return;
     const int s = wid / a.num_heads;
@@ -330,96 +341,108 @@ extern "C" size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads,
     return sp_layout(num_seqs, num_heads, head_dim, z.slots).total;
 }
 
-extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
-    const pkv_pool *pool, void *out, pkv_dtype out_dtype, const void *query, int num_seqs,
-    int num_heads, int num_kv_heads, const int32_t *block_tables, int max_blocks_per_seq,
-    const int32_t *context_lens, int max_context_len, float scale, const int32_t *group_starts,
-    const int32_t *prefix_lens, int num_groups, int max_prefix_len, int partition_tokens,
-    void *workspace, size_t workspace_bytes, void *stream) {
+namespace pkv {
+namespace {
+
+// Host-side checks and sizes shared by the plan, the run and the combined call.
+struct SpCall {
+    int BS, group, dev, ctx_cap, maxp, cap_blocks;
+    SpSizes z;
+    SpLayout lay;
+};
+
+pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num_kv_heads,
+                      int max_blocks_per_seq, int max_context_len, int max_prefix_len,
+                      int partition_tokens, void *workspace, size_t workspace_bytes, SpCall &c) {
     if (!pool || pool->magic != kPoolMagic || pool->layout != 0) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
         max_context_len < 0 || max_prefix_len < 0)
         return PKV_ERR_INVALID_ARG;
     if (num_kv_heads != pool->num_kv_heads || num_heads % num_kv_heads != 0)
         return PKV_ERR_INVALID_ARG;
-    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
-    const int BS = pool->block_size;
+    c.BS = pool->block_size;
     if (partition_tokens < -1 || partition_tokens > kMaxPartitionTokens ||
-        (partition_tokens > 0 && partition_tokens % BS != 0))
+        (partition_tokens > 0 && partition_tokens % c.BS != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    if (num_groups < 1 || num_groups > num_seqs) return PKV_ERR_INVALID_ARG;
-    if (!out || !query || !block_tables || !context_lens || !group_starts || !prefix_lens)
-        return PKV_ERR_INVALID_ARG;
-    if (!aligned(out, 16) || !aligned(query, 16) || !aligned(block_tables, 4) ||
-        !aligned(context_lens, 4) || !aligned(group_starts, 4) || !aligned(prefix_lens, 4))
-        return PKV_ERR_INVALID_ARG;
     if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    const int group = num_heads / num_kv_heads;
-    if (group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
-    int dev = 0;
-    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
-    if (dev != pool->device) return PKV_ERR_INVALID_ARG;
-
-    const SpSizes z = sp_sizes(partition_tokens, max_context_len, max_prefix_len);
-    const SpLayout lay = sp_layout(num_seqs, num_heads, pool->head_dim, z.slots);
-    if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
+    c.group = num_heads / num_kv_heads;
+    if (c.group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
+    c.z = sp_sizes(partition_tokens, max_context_len, max_prefix_len);
+    c.lay = sp_layout(num_seqs, num_heads, pool->head_dim, c.z.slots);
+    if (!workspace || workspace_bytes < c.lay.total) return PKV_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
-    const long long max_entries = (long long)num_seqs * z.slots;
-    if (max_entries * kMaxGroup * num_kv_heads >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * c.z.slots * kMaxGroup * num_kv_heads >= (1ll << 31))
+        return PKV_ERR_UNSUPPORTED;
+    const long long table_cap = (long long)max_blocks_per_seq * c.BS;
+    c.ctx_cap = (int)(table_cap < max_context_len ? table_cap : max_context_len);
+    c.maxp = max_prefix_len < max_context_len ? max_prefix_len : max_context_len;
+    c.cap_blocks = (c.ctx_cap + c.BS - 1) / c.BS;
+    if (cuda_status(cudaGetDevice(&c.dev)) != PKV_OK) return PKV_ERR_CUDA;
+    if (c.dev != pool->device) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
 
-    const long long table_cap = (long long)max_blocks_per_seq * BS;
-    const int ctx_cap = (int)(table_cap < max_context_len ? table_cap : max_context_len);
-    const int maxp = max_prefix_len < max_context_len ? max_prefix_len : max_context_len;
-    const int cap_blocks = (ctx_cap + BS - 1) / BS;
+pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_heads,
+                   const int32_t *context_lens, const int32_t *group_starts,
+                   const int32_t *prefix_lens, int num_groups, void *workspace, cudaStream_t st) {
     char *ws = static_cast<char *>(workspace);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-
     SpPlan p;
     std::memset(&p, 0, sizeof(p));
     p.group_starts = group_starts;
     p.prefix_lens = prefix_lens;
     p.context_lens = context_lens;
     p.dev_error = pool->dev_error;
-    p.entries = reinterpret_cast<SpEntry *>(ws + lay.entries);
-    p.nparts = reinterpret_cast<int32_t *>(ws + lay.nparts);
-    p.share = reinterpret_cast<int32_t *>(ws + lay.share);
-    p.header = reinterpret_cast<int32_t *>(ws + lay.header);
+    p.entries = reinterpret_cast<SpEntry *>(ws + c.lay.entries);
+    p.nparts = reinterpret_cast<int32_t *>(ws + c.lay.nparts);
+    p.share = reinterpret_cast<int32_t *>(ws + c.lay.share);
+    p.header = reinterpret_cast<int32_t *>(ws + c.lay.header);
     p.num_groups = num_groups;
     p.num_seqs = num_seqs;
-    p.ctx_cap = ctx_cap;
-    p.max_prefix_len = maxp;
-    p.block_size = BS;
-    p.pbp = z.ptp > 0 ? z.ptp / BS : ((maxp + BS - 1) / BS > 0 ? (maxp + BS - 1) / BS : 1);
-    p.pbs = z.pts > 0 ? z.pts / BS : (cap_blocks > 0 ? cap_blocks : 1);
-    p.members_per_item = kSpRowsMax / group;
-    p.prefix_cap = num_seqs * z.pp;
-    p.suffix_cap = num_seqs * z.ps;
+    p.num_heads = num_heads;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.slots = c.z.slots;
+    p.ctx_cap = c.ctx_cap;
+    p.max_prefix_len = c.maxp;
+    p.block_size = c.BS;
+    p.pbp = c.z.ptp > 0 ? c.z.ptp / c.BS
+                        : ((c.maxp + c.BS - 1) / c.BS > 0 ? (c.maxp + c.BS - 1) / c.BS : 1);
+    p.pbs = c.z.pts > 0 ? c.z.pts / c.BS : (c.cap_blocks > 0 ? c.cap_blocks : 1);
+    p.members_per_item = kSpRowsMax / c.group;
+    p.prefix_cap = num_seqs * c.z.pp;
+    p.suffix_cap = num_seqs * c.z.ps;
     shared_prefix_plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
-    if (cuda_status(cudaGetLastError()) != PKV_OK) return PKV_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
+}
 
+pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype out_dtype,
+                  const void *query, int num_seqs, int num_heads, const int32_t *block_tables,
+                  int max_blocks_per_seq, float scale, void *workspace, cudaStream_t st) {
+    char *ws = static_cast<char *>(workspace);
     SpArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q = query;
     a.out = out;
-    a.ws_o = reinterpret_cast<float *>(ws + lay.o);
-    a.ws_lse = reinterpret_cast<float *>(ws + lay.lse);
+    a.ws_o = reinterpret_cast<float *>(ws + c.lay.o);
+    a.ws_lse = reinterpret_cast<float *>(ws + c.lay.lse);
     a.block_tables = block_tables;
     a.dev_error = pool->dev_error;
-    a.entries = p.entries;
-    a.nparts = p.nparts;
-    a.seq_share = p.share;
+    a.entries = reinterpret_cast<const SpEntry *>(ws + c.lay.entries);
+    a.nparts = reinterpret_cast<const int32_t *>(ws + c.lay.nparts);
+    a.seq_share = reinterpret_cast<const int32_t *>(ws + c.lay.share);
     a.block_tables_chk = block_tables;
-    a.counter = p.header + 2;
-    a.count = p.header;
-    a.suffix_base = p.prefix_cap;
+    int32_t *header = reinterpret_cast<int32_t *>(ws + c.lay.header);
+    a.counter = header + 2;
+    a.count = header;
+    a.suffix_base = num_seqs * c.z.pp;
+    a.num_seqs = num_seqs;
     a.num_heads = num_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.group = group;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.group = c.group;
+    a.block_size = c.BS;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = pool->num_blocks;
-    a.num_slots = z.slots;
+    a.num_slots = c.z.slots;
     a.out_bf16 = out_dtype == PKV_BF16;
     a.scale_log2 = scale * 1.4426950408889634f;
 
@@ -430,18 +453,100 @@ extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
     L.tmv = &maps[1];
     L.args = a;
     L.head_dim = pool->head_dim;
-    L.block_size = BS;
+    L.block_size = c.BS;
     L.stream = st;
-    L.device = dev;
+    L.device = c.dev;
     const pkv_status s1 =
         pool->head_dim == 64 ? launch_shared_prefix_d64(L) : launch_shared_prefix_d128(L);
     if (s1 != PKV_OK) return s1;
 
-    // the combine waits for the decode grid in griddepcontrol.wait
+    // the combine waits for the decode grid in griddepcontrol.wait, then
+    // resets the work counter for the next run on the same plan
     const dim3 cgrid((unsigned)(((long long)num_seqs * num_heads + 7) / 8));
     if (pool->head_dim == 64)
         return cuda_status(
             launch_dependent(shared_prefix_combine_kernel<64>, cgrid, dim3(256), 0, st, a, num_seqs));
     return cuda_status(
         launch_dependent(shared_prefix_combine_kernel<128>, cgrid, dim3(256), 0, st, a, num_seqs));
+}
+
+bool sp_out_args_ok(void *out, pkv_dtype out_dtype, const void *query, const int32_t *block_tables,
+                    float scale) {
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return false;
+    if (!std::isfinite(scale)) return false;
+    if (!out || !query || !block_tables) return false;
+    return aligned(out, 16) && aligned(query, 16) && aligned(block_tables, 4);
+}
+
+bool sp_plan_args_ok(const int32_t *context_lens, const int32_t *group_starts,
+                     const int32_t *prefix_lens, int num_groups, int num_seqs) {
+    if (num_groups < 1 || num_groups > num_seqs) return false;
+    if (!context_lens || !group_starts || !prefix_lens) return false;
+    return aligned(context_lens, 4) && aligned(group_starts, 4) && aligned(prefix_lens, 4);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_shared_prefix_plan(const pkv_pool *pool, int num_seqs, int num_heads,
+                                             int num_kv_heads, int max_blocks_per_seq,
+                                             const int32_t *context_lens, int max_context_len,
+                                             const int32_t *group_starts,
+                                             const int32_t *prefix_lens, int num_groups,
+                                             int max_prefix_len, int partition_tokens,
+                                             void *workspace, size_t workspace_bytes,
+                                             void *stream) {
+    // host-only checks first: nothing below them touches the device
+    if (pool && pool->magic == kPoolMagic && num_seqs > 0 &&
+        !sp_plan_args_ok(context_lens, group_starts, prefix_lens, num_groups, num_seqs))
+        return PKV_ERR_INVALID_ARG;
+    SpCall c;
+    const pkv_status st =
+        sp_prepare(pool, num_seqs, num_heads, num_kv_heads, max_blocks_per_seq, max_context_len,
+                   max_prefix_len, partition_tokens, workspace, workspace_bytes, c);
+    if (st != PKV_OK || num_seqs == 0) return st;
+    return sp_plan(pool, c, num_seqs, num_heads, context_lens, group_starts, prefix_lens,
+                   num_groups, workspace, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_shared_prefix_run(
+    const pkv_pool *pool, void *out, pkv_dtype out_dtype, const void *query, int num_seqs,
+    int num_heads, int num_kv_heads, const int32_t *block_tables, int max_blocks_per_seq,
+    int max_context_len, float scale, int max_prefix_len, int partition_tokens, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    // host-only checks first: nothing below them touches the device
+    if (pool && pool->magic == kPoolMagic && num_seqs > 0 &&
+        !sp_out_args_ok(out, out_dtype, query, block_tables, scale))
+        return PKV_ERR_INVALID_ARG;
+    SpCall c;
+    const pkv_status st =
+        sp_prepare(pool, num_seqs, num_heads, num_kv_heads, max_blocks_per_seq, max_context_len,
+                   max_prefix_len, partition_tokens, workspace, workspace_bytes, c);
+    if (st != PKV_OK || num_seqs == 0) return st;
+    return sp_run(pool, c, out, out_dtype, query, num_seqs, num_heads, block_tables,
+                  max_blocks_per_seq, scale, workspace, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_shared_prefix(
+    const pkv_pool *pool, void *out, pkv_dtype out_dtype, const void *query, int num_seqs,
+    int num_heads, int num_kv_heads, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, float scale, const int32_t *group_starts,
+    const int32_t *prefix_lens, int num_groups, int max_prefix_len, int partition_tokens,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    if (pool && pool->magic == kPoolMagic && num_seqs > 0) {
+        if (!sp_out_args_ok(out, out_dtype, query, block_tables, scale)) return PKV_ERR_INVALID_ARG;
+        if (!sp_plan_args_ok(context_lens, group_starts, prefix_lens, num_groups, num_seqs))
+            return PKV_ERR_INVALID_ARG;
+    }
+    SpCall c;
+    const pkv_status st =
+        sp_prepare(pool, num_seqs, num_heads, num_kv_heads, max_blocks_per_seq, max_context_len,
+                   max_prefix_len, partition_tokens, workspace, workspace_bytes, c);
+    if (st != PKV_OK || num_seqs == 0) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const pkv_status sp = sp_plan(pool, c, num_seqs, num_heads, context_lens, group_starts,
+                                  prefix_lens, num_groups, workspace, s);
+    if (sp != PKV_OK) return sp;
+    return sp_run(pool, c, out, out_dtype, query, num_seqs, num_heads, block_tables,
+                  max_blocks_per_seq, scale, workspace, s);
 }

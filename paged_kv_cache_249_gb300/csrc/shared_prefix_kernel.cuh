@@ -250,7 +250,9 @@ __global__ void __launch_bounds__(kSpWarps * 32)
     }
     __syncwarp();
     griddep_wait();  // the work list of the planning kernel is complete and visible
-    const int nP = a.count[0], nS = a.count[1];
+    const bool planned = sp_plan_matches(a);
+    if (!planned && blockIdx.x == 0 && threadIdx.x == 0) raise_fault(a.dev_error, PKV_FAULT_PREFIX);
+    const int nP = planned ? a.count[0] : 0, nS = planned ? a.count[1] : 0;
     const int totalP = nP * Hkv, total = (nP + nS) * Hkv;
 
     auto fetch = [&]() -> int {

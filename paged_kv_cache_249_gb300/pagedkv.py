@@ -36,7 +36,8 @@ EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_bm_context_len", "pkv_bm_pending_copies", "pkv_bm_take_copies",
            "pkv_bm_block_tables", "pkv_contiguous_cache_init",
            "pkv_contiguous_attention_decode", "pkv_shared_prefix_workspace_bytes",
-           "pkv_paged_attention_decode_shared_prefix"]
+           "pkv_paged_attention_decode_shared_prefix", "pkv_shared_prefix_plan",
+           "pkv_paged_attention_decode_shared_prefix_run"]
 
 
 class PagedKVError(RuntimeError):
@@ -86,6 +87,9 @@ def load(path: Optional[str] = None):
         "pkv_shared_prefix_workspace_bytes": (Z, [I, I, I, I, I, I]),
         "pkv_paged_attention_decode_shared_prefix": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, P, P,
                                                          I, I, I, P, Z, P]),
+        "pkv_shared_prefix_plan": (I, [PP, I, I, I, I, P, I, P, P, I, I, I, P, Z, P]),
+        "pkv_paged_attention_decode_shared_prefix_run": (I, [PP, P, I, P, I, I, I, P, I, I, F, I, I,
+                                                             P, Z, P]),
         "pkv_bm_create": (I, [I, I, ctypes.POINTER(P)]),
         "pkv_bm_destroy": (None, [P]),
         "pkv_bm_free_blocks": (I, [P]),
@@ -272,6 +276,39 @@ def paged_attention_decode_shared_prefix(pool: BlockPool, out: torch.Tensor, que
         group_starts.data_ptr(), prefix_lens.data_ptr(), prefix_lens.numel(),
         int(max_prefix_len), int(partition_tokens), workspace.data_ptr(), ws_bytes,
         _stream(stream)), "pkv_paged_attention_decode_shared_prefix")
+
+
+def shared_prefix_plan(pool: BlockPool, num_heads: int, context_lens: torch.Tensor,
+                       max_context_len: int, group_starts: torch.Tensor,
+                       prefix_lens: torch.Tensor, max_prefix_len: int, workspace: torch.Tensor,
+                       max_blocks_per_seq: int, num_kv_heads: Optional[int] = None,
+                       partition_tokens: int = 0, stream=None) -> None:
+    """pkv_shared_prefix_plan: the work list of a shared-prefix decode, reusable
+    by every layer of the step."""
+    _check(load().pkv_shared_prefix_plan(
+        ctypes.byref(pool.desc), context_lens.numel(), num_heads,
+        num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, int(max_blocks_per_seq),
+        context_lens.data_ptr(), int(max_context_len), group_starts.data_ptr(),
+        prefix_lens.data_ptr(), prefix_lens.numel(), int(max_prefix_len), int(partition_tokens),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "pkv_shared_prefix_plan")
+
+
+def paged_attention_decode_shared_prefix_run(pool: BlockPool, out: torch.Tensor,
+                                             query: torch.Tensor, block_tables: torch.Tensor,
+                                             max_context_len: int, scale: float,
+                                             max_prefix_len: int, workspace: torch.Tensor,
+                                             num_kv_heads: Optional[int] = None,
+                                             partition_tokens: int = 0, stream=None) -> None:
+    """pkv_paged_attention_decode_shared_prefix_run: decode from the plan in
+    `workspace`."""
+    S, H, _ = query.shape
+    _check(load().pkv_paged_attention_decode_shared_prefix_run(
+        ctypes.byref(pool.desc), out.data_ptr(), _dtype_code(out.dtype), query.data_ptr(), S, H,
+        num_kv_heads if num_kv_heads is not None else pool.num_kv_heads, block_tables.data_ptr(),
+        block_tables.shape[1], int(max_context_len), float(scale), int(max_prefix_len),
+        int(partition_tokens), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "pkv_paged_attention_decode_shared_prefix_run")
 
 
 class ContiguousCache:
@@ -470,4 +507,17 @@ class DeviceWorkload:
         paged_attention_decode_shared_prefix(
             self.pool, self.out, self.q, self.block_tables, self.context_lens,
             self.max_context_len, self.w.scale, self.group_starts, self.prefix_lens,
+            self.max_prefix_len, self.sp_workspace, self.w.num_kv_heads, self.sp_partition, stream)
+
+    def shared_prefix_plan(self, stream=None) -> None:
+        if not hasattr(self, "sp_workspace"):
+            self.shared_prefix_setup()
+        shared_prefix_plan(self.pool, self.w.num_heads, self.context_lens, self.max_context_len,
+                           self.group_starts, self.prefix_lens, self.max_prefix_len,
+                           self.sp_workspace, self.block_tables.shape[1], self.w.num_kv_heads,
+                           self.sp_partition, stream)
+
+    def decode_shared_prefix_run(self, stream=None) -> None:
+        paged_attention_decode_shared_prefix_run(
+            self.pool, self.out, self.q, self.block_tables, self.max_context_len, self.w.scale,
             self.max_prefix_len, self.sp_workspace, self.w.num_kv_heads, self.sp_partition, stream)

@@ -210,3 +210,43 @@ def test_shared_prefix_workspace_bytes(lib):
         assert f(S, H, D, maxc, maxp, pt) == expect(S, H, D, maxc, maxp, pt), (S, maxc, maxp, pt)
     assert f(0, 8, 128, 100, 0, 0) == 0
     assert f(4, 8, 128, 100, -1, 0) == 0
+
+
+def test_shared_prefix_plan_and_run_reject_bad_arguments_on_host(lib):
+    E, U = pagedkv.ERR_INVALID_ARG, pagedkv.ERR_UNSUPPORTED
+    pool = _fake_pool()
+
+    def plan(p, **kw):
+        a = dict(S=4, H=8, Hkv=2, MB=8, cl=0x4000, maxc=128, gs=0x5000, pl=0x6000, ng=2, maxp=64,
+                 pt=0, ws=0x7000, wsb=1 << 20)
+        a.update(kw)
+        return lib.pkv_shared_prefix_plan(
+            ctypes.byref(p) if p is not None else None, a["S"], a["H"], a["Hkv"], a["MB"],
+            a["cl"], a["maxc"], a["gs"], a["pl"], a["ng"], a["maxp"], a["pt"], a["ws"], a["wsb"],
+            None)
+
+    def run(p, **kw):
+        a = dict(out=0x1000, dt=pagedkv.F32, q=0x2000, S=4, H=8, Hkv=2, bt=0x3000, MB=8,
+                 maxc=128, scale=0.1, maxp=64, pt=0, ws=0x7000, wsb=1 << 20)
+        a.update(kw)
+        return lib.pkv_paged_attention_decode_shared_prefix_run(
+            ctypes.byref(p) if p is not None else None, a["out"], a["dt"], a["q"], a["S"], a["H"],
+            a["Hkv"], a["bt"], a["MB"], a["maxc"], a["scale"], a["maxp"], a["pt"], a["ws"],
+            a["wsb"], None)
+
+    assert plan(None) == E
+    assert plan(pool, ng=0) == E
+    assert plan(pool, cl=0) == E
+    assert plan(pool, gs=0x5002) == E
+    assert plan(pool, pt=24) == E
+    assert plan(pool, wsb=16) == pagedkv.ERR_WORKSPACE
+    assert plan(_fake_pool(dtype=pagedkv.F32)) == U
+    assert plan(pool, S=0) == pagedkv.OK
+    assert run(None) == E
+    assert run(pool, out=0) == E
+    assert run(pool, q=0x2008) == E
+    assert run(pool, scale=float("nan")) == E
+    assert run(pool, dt=9) == E
+    assert run(pool, H=34) == U
+    assert run(pool, ws=0x7010) == E                                  # not 256-byte aligned
+    assert run(pool, S=0) == pagedkv.OK

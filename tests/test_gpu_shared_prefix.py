@@ -170,3 +170,42 @@ def test_fullsize_shared_prefix_workload_sampled():
                  "shared_prefix workload")
     # every sequence agrees with the plain kernel to within both tolerances
     assert float((dw.out.float() - plain.float()).abs().max()) <= 4e-3 + 2 ** -8
+
+
+# ---------------------------------------------------- plan once, run per layer
+
+def test_one_plan_serves_several_layers():
+    """A model's layers share the step's batch: plan once, run per layer with
+    that layer's queries (here: the same pool, new queries each time)."""
+    ctx, groups, H, Hkv, D, BS = CASES["g4_ragged_groups"]
+    w = _w("layers", ctx, groups, H, Hkv, D, BS, seed=21)
+    dw = pagedkv.DeviceWorkload(w)
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    dw.shared_prefix_setup(partition_tokens=64)
+    dw.shared_prefix_plan()
+    g = torch.Generator().manual_seed(5)
+    for layer in range(4):
+        q = torch.randn(w.q.shape, generator=g).to(torch.bfloat16)
+        dw.q.copy_(q)
+        dw.decode_shared_prefix_run()
+        torch.cuda.synchronize()
+        assert pagedkv.get_device_error(dw.pool) == 0
+        w.q = q
+        ref, _, _ = oracle_after_write(w)
+        assert_close(dw.out, ref, "bf16", f"layer {layer}")
+
+
+def test_run_without_or_against_another_plan_is_reported():
+    ctx, groups, H, Hkv, D, BS = CASES["g4_eight_members"]
+    w = _w("noplan", ctx, groups, H, Hkv, D, BS, seed=22)
+    dw = pagedkv.DeviceWorkload(w)
+    dw.shared_prefix_setup(partition_tokens=0)
+    dw.sp_workspace.zero_()
+    dw.out.fill_(7.0)
+    dw.decode_shared_prefix_run()  # no plan in the workspace
+    assert pagedkv.get_device_error(dw.pool) & pagedkv.FAULT_PREFIX
+    assert float(dw.out.min()) == 7.0 == float(dw.out.max())  # nothing written
+    dw.shared_prefix_plan()
+    dw.sp_partition = -1  # a run with another geometry than the plan's (fits the workspace)
+    dw.decode_shared_prefix_run()
+    assert pagedkv.get_device_error(dw.pool) & pagedkv.FAULT_PREFIX
