@@ -41,11 +41,13 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum), keyed by workload, valid only while the kernel
 # sources hash to `src`.  Filled in from the profiles summaries.
 NCU_TRAFFIC: dict = {
-    # profiles/paged_decode_kernel_mha_7b_gqa_8b.md
-    ("mha_7b", "plain"): {"bytes": 1105898000 + 5509888, "src": "e8c95f027e4ecfd6"},
-    ("gqa_8b", "plain"): {"bytes": 2374323000 + 13362432, "src": "e8c95f027e4ecfd6"},
-    # profiles/shared_prefix_decode_kernel_shared_prefix.md
-    ("shared_prefix", "shared"): {"bytes": 856257024 + 40258048, "src": "174fcd69097c2fe0"},
+    # profiles/paged_decode_kernel_mha_7b_gqa_8b_long_ctx.md
+    ("mha_7b", "plain"): {"bytes": 1105862000 + 5882624, "src": "57b8efbe4f5d189d"},
+    ("gqa_8b", "plain"): {"bytes": 2374026000 + 13411840, "src": "57b8efbe4f5d189d"},
+    ("long_ctx", "plain"): {"bytes": 2975526000 + 48092416, "src": "57b8efbe4f5d189d"},
+    # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
+    # include the plain kernel's header, so a change there re-dates it)
+    ("shared_prefix", "shared"): {"bytes": 856257024 + 40258048, "src": "SHARED_STALE"},
 }
 
 

@@ -166,7 +166,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
  * workspace: device buffer of at least pkv_decode_workspace_bytes(...) bytes
  *   when a split can happen (may be NULL with partition_tokens = -1).
  * flags: one of PKV_DECODE_PATH_*.
- * Supported groups: num_heads / num_kv_heads in 1..16.
+ * Supported groups: num_heads / num_kv_heads in 1..16; num_seqs <= 65535.
  */
 pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype out_dtype,
                                       const void *query, int num_seqs, int num_heads,

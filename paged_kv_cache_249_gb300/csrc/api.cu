@@ -250,7 +250,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
         return PKV_ERR_INVALID_ARG;
     const int group = num_heads / num_kv_heads;
     if (group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
-    if (num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (num_kv_heads > 65535 || num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid y
     const bool bf16 = pool->dtype == PKV_BF16;
     bool mma = bf16 && group >= 4;
     if (flags == PKV_DECODE_PATH_FMA) mma = false;

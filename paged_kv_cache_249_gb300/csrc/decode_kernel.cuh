@@ -461,7 +461,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-    const int s = blockIdx.x, g = blockIdx.y, part = blockIdx.z;
+    // kv head fastest: consecutive CTAs read neighbouring (block, kv head) tiles
+    const int g = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     griddep_wait();  // inputs written by the kernel before this one are complete
 
@@ -624,7 +625,7 @@ pkv_status launch_one(const DecodeLaunch &L) {
             return PKV_ERR_CUDA;
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
     }
-    dim3 grid(L.num_seqs, L.args.num_kv_heads, L.args.num_parts);
+    dim3 grid(L.args.num_kv_heads, L.num_seqs, L.args.num_parts);
     return cuda_status(
         launch_dependent(kern, grid, dim3(kDecodeWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }
