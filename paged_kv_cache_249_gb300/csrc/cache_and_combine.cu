@@ -118,9 +118,10 @@ struct CombRow {
     const float *lse, *po;
 };
 
-__device__ __forceinline__ CombRow comb_row(const DecodeArgs &a, int head_dim, int block_size) {
+__device__ __forceinline__ CombRow comb_row(const DecodeArgs &a, int head_dim, int block_size,
+                                            int sh) {
     CombRow r;
-    r.sh = blockIdx.x;  // s * H + h
+    r.sh = sh;  // s * H + h
     const int s = r.sh / a.num_heads;
     int ctx = __ldg(a.context_lens + s);
     ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kCombThreads)
     lse_combine_kernel(const DecodeArgs a, int head_dim, int block_size) {
     __shared__ float red[kCombThreads / 32];
     griddep_wait();  // the decode grid's partials are complete
-    const CombRow r = comb_row(a, head_dim, block_size);
+    const CombRow r = comb_row(a, head_dim, block_size, blockIdx.x);
     if (r.nparts <= 1) return;  // the decode kernel wrote this row directly
     const float M = comb_max(r, red);
     for (int d = threadIdx.x; d < head_dim; d += kCombThreads) {
@@ -173,23 +174,27 @@ __global__ void __launch_bounds__(kCombThreads)
     }
 }
 
-// Many partitions (a long context has hundreds): the weights 2^(lse_p - M)
-// are computed once into shared memory, kCombChunk parts at a time, and
-// every column is summed over the parts with eight independent loads in
-// flight per thread (head_dim 64: two threads per column, each every other
-// part).
+// Many partitions (a long context has hundreds): each (sequence, head) is
+// split over head_dim/32 CTAs of 32 columns, so the reads of the partials
+// have enough CTAs in flight.  A CTA computes the weights 2^(lse_p - M) once
+// into shared memory, kCombChunk parts at a time; four part groups of 32
+// threads then sum their columns over every fourth part, with eight
+// independent loads in flight per thread.
+constexpr int kCombCols = 32;
+constexpr int kCombGroups = kCombThreads / kCombCols;
+
 __global__ void __launch_bounds__(kCombThreads)
     lse_combine_many_kernel(const DecodeArgs a, int head_dim, int block_size) {
     __shared__ float w_s[kCombChunk];
     __shared__ float red_m[kCombThreads / 32], red_d[kCombThreads / 32];
     __shared__ float acc_s[kCombThreads];
     griddep_wait();  // the decode grid's partials are complete
-    const CombRow r = comb_row(a, head_dim, block_size);
+    const int slices = head_dim / kCombCols;
+    const CombRow r = comb_row(a, head_dim, block_size, blockIdx.x / slices);
     if (r.nparts <= 1) return;  // the decode kernel wrote this row directly
     const float M = comb_max(r, red_m);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tpc = kCombThreads / head_dim;
-    const int d = tid % head_dim, pg = tid / head_dim;
+    const int d = (blockIdx.x % slices) * kCombCols + (tid % kCombCols), pg = tid / kCombCols;
     float num = 0.f, den = 0.f;
     for (int p0 = 0; p0 < r.nparts; p0 += kCombChunk) {
         const int n = r.nparts - p0 < kCombChunk ? r.nparts - p0 : kCombChunk;
@@ -202,14 +207,14 @@ __global__ void __launch_bounds__(kCombThreads)
         __syncthreads();
         const float *col = r.po + (size_t)p0 * head_dim + d;
         int i = pg;
-        for (; i + 7 * tpc < n; i += 8 * tpc) {
+        for (; i + 7 * kCombGroups < n; i += 8 * kCombGroups) {
             float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = col[(size_t)(i + u * tpc) * head_dim];
+            for (int u = 0; u < 8; ++u) v[u] = col[(size_t)(i + u * kCombGroups) * head_dim];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) num = fmaf(w_s[i + u * tpc], v[u], num);
+            for (int u = 0; u < 8; ++u) num = fmaf(w_s[i + u * kCombGroups], v[u], num);
         }
-        for (; i < n; i += tpc) num = fmaf(w_s[i], col[(size_t)i * head_dim], num);
+        for (; i < n; i += kCombGroups) num = fmaf(w_s[i], col[(size_t)i * head_dim], num);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
@@ -220,7 +225,8 @@ __global__ void __launch_bounds__(kCombThreads)
     den = 0.f;
 #pragma unroll
     for (int w = 0; w < kCombThreads / 32; ++w) den += red_d[w];
-    for (int q = 1; q < tpc; ++q) num += acc_s[d + q * head_dim];
+#pragma unroll
+    for (int q = 1; q < kCombGroups; ++q) num += acc_s[tid + q * kCombCols];
     comb_store(a, (size_t)r.sh * head_dim + d, den > 0.f ? num / den : 0.f);
 }
 
@@ -228,9 +234,12 @@ pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, i
                               cudaStream_t stream) {
     const long long n = (long long)num_seqs * a.num_heads;
     if (n == 0) return PKV_OK;
-    auto kern = a.num_parts <= kCombDirect ? lse_combine_kernel : lse_combine_many_kernel;
-    return cuda_status(launch_dependent(kern, dim3((unsigned)n), dim3(kCombThreads), 0, stream, a,
-                                        head_dim, block_size));
+    if (a.num_parts <= kCombDirect)
+        return cuda_status(launch_dependent(lse_combine_kernel, dim3((unsigned)n),
+                                            dim3(kCombThreads), 0, stream, a, head_dim, block_size));
+    return cuda_status(launch_dependent(lse_combine_many_kernel,
+                                        dim3((unsigned)(n * (head_dim / kCombCols))),
+                                        dim3(kCombThreads), 0, stream, a, head_dim, block_size));
 }
 
 }  // namespace pkv
