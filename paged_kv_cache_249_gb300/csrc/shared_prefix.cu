@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     // the decode kernel may start setting up; it waits for this grid in
     // griddepcontrol.wait before it reads anything written here
     griddep_launch();
+    griddep_wait();  // inputs written by the kernel before this one are complete
     const int tid = threadIdx.x;
     const bool staged = p.num_seqs <= kPlanSmemSeqs;
     bool bad = false;
@@ -411,8 +412,7 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
     p.members_per_item = kSpRowsMax / c.group;
     p.prefix_cap = num_seqs * c.z.pp;
     p.suffix_cap = num_seqs * c.z.ps;
-    shared_prefix_plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_dependent(shared_prefix_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, p));
 }
 
 pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype out_dtype,
