@@ -365,6 +365,16 @@ pkv_status pkv_bm_block_tables(const pkv_block_manager *bm, const int64_t *seq_i
                                int max_blocks_per_seq, int32_t *block_tables,
                                int32_t *context_lens);
 
+/* Group description for the shared-prefix decode: for each group of the
+ * listed sequences (group g = seq_ids[group_starts[g] .. group_starts[g+1]),
+ * host arrays), prefix_lens[g] receives the tokens of the longest run of
+ * leading blocks that every member holds in its table and has filled
+ * (0 for a group of one).  Sequences forked from one prompt and listed side
+ * by side make a group. */
+pkv_status pkv_bm_shared_prefix(const pkv_block_manager *bm, const int64_t *seq_ids, int num_seqs,
+                                const int32_t *group_starts, int num_groups,
+                                int32_t *prefix_lens);
+
 /*
  * Synchronise `stream`, read the pool's device error word into *fault_bits
  * (may be NULL) and clear it.  Returns PKV_ERR_DEVICE_FAULT if it was

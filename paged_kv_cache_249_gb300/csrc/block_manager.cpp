@@ -13,6 +13,8 @@
 // Host memory only; no CUDA call.  Not thread-safe: one manager per thread
 // or external locking.
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <new>
 #include <unordered_map>
 #include <utility>
@@ -180,6 +182,42 @@ pkv_status pkv_bm_block_tables(const pkv_block_manager *bm, const int64_t *seq_i
         std::fill(row, row + max_blocks_per_seq, -1);
         std::copy(seq.blocks.begin(), seq.blocks.end(), row);
         context_lens[i] = (int32_t)seq.len;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_bm_shared_prefix(const pkv_block_manager *bm, const int64_t *seq_ids, int num_seqs,
+                                const int32_t *group_starts, int num_groups,
+                                int32_t *prefix_lens) {
+    if (!bm || num_seqs < 0 || num_groups < 0) return PKV_ERR_INVALID_ARG;
+    if (num_groups == 0) return num_seqs == 0 ? PKV_OK : PKV_ERR_INVALID_ARG;
+    if (!group_starts || !prefix_lens || (num_seqs > 0 && !seq_ids)) return PKV_ERR_INVALID_ARG;
+    if (group_starts[0] != 0 || group_starts[num_groups] != num_seqs) return PKV_ERR_INVALID_ARG;
+    std::vector<const pkv_block_manager::Seq *> rows((size_t)num_seqs);
+    for (int i = 0; i < num_seqs; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
+        rows[(size_t)i] = &it->second;
+    }
+    for (int g = 0; g < num_groups; ++g)
+        if (group_starts[g] > group_starts[g + 1]) return PKV_ERR_INVALID_ARG;
+    for (int g = 0; g < num_groups; ++g) {
+        const int a = group_starts[g], b = group_starts[g + 1];
+        int64_t common = 0;
+        if (b - a >= 2) {
+            // leading blocks that every member holds, full in every member
+            int64_t full = INT64_MAX;
+            for (int i = a; i < b; ++i) full = std::min(full, rows[(size_t)i]->len / bm->block_size);
+            while (common < full) {
+                const int32_t blk = rows[(size_t)a]->blocks[(size_t)common];
+                bool same = true;
+                for (int i = a + 1; i < b && same; ++i) same = rows[(size_t)i]->blocks[(size_t)common] == blk;
+                if (!same) break;
+                ++common;
+            }
+        }
+        const int64_t tokens = common * bm->block_size;
+        prefix_lens[g] = tokens > INT32_MAX ? INT32_MAX / bm->block_size * bm->block_size : (int32_t)tokens;
     }
     return PKV_OK;
 }

@@ -34,7 +34,7 @@ EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_free_blocks", "pkv_bm_refcount",
            "pkv_bm_add_sequence", "pkv_bm_fork", "pkv_bm_append_token", "pkv_bm_free_sequence",
            "pkv_bm_context_len", "pkv_bm_pending_copies", "pkv_bm_take_copies",
-           "pkv_bm_block_tables", "pkv_contiguous_cache_init",
+           "pkv_bm_block_tables", "pkv_bm_shared_prefix", "pkv_contiguous_cache_init",
            "pkv_contiguous_attention_decode", "pkv_shared_prefix_workspace_bytes",
            "pkv_paged_attention_decode_shared_prefix", "pkv_shared_prefix_plan",
            "pkv_paged_attention_decode_shared_prefix_run"]
@@ -102,6 +102,7 @@ def load(path: Optional[str] = None):
         "pkv_bm_pending_copies": (I, [P]),
         "pkv_bm_take_copies": (I, [P, P, P, I]),
         "pkv_bm_block_tables": (I, [P, P, I, I, P, P]),
+        "pkv_bm_shared_prefix": (I, [P, P, I, P, I, P]),
         "pkv_status_string": (ctypes.c_char_p, [I]),
         "pkv_last_cuda_error": (ctypes.c_char_p, []),
         "pkv_version": (I, []),
@@ -430,6 +431,16 @@ class BlockManager:
                                             bt.ctypes.data, cl.ctypes.data),
                "pkv_bm_block_tables")
         return bt, cl
+
+    def shared_prefix(self, seq_ids, group_starts) -> np.ndarray:
+        """Tokens of the leading full blocks each group's members share."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        gs = np.ascontiguousarray(group_starts, dtype=np.int32)
+        out = np.zeros(max(gs.size - 1, 1), dtype=np.int32)
+        _check(self.lib.pkv_bm_shared_prefix(self.h, ids.ctypes.data, ids.size, gs.ctypes.data,
+                                             gs.size - 1, out.ctypes.data),
+               "pkv_bm_shared_prefix")
+        return out[:gs.size - 1]
 
 
 def get_device_error(pool: BlockPool, stream=None) -> int:

@@ -138,3 +138,31 @@ def test_invalid_arguments():
         assert e.value.status == pagedkv.ERR_INVALID_ARG
     with pytest.raises(pagedkv.PagedKVError):
         bm.block_tables([1], 0)
+
+
+def test_shared_prefix_of_forked_sequences():
+    """Forked sequences share their parent's full blocks; a partly filled
+    last block is not counted, and copy-on-write does not change the count
+    of full shared blocks."""
+    bm = pagedkv.BlockManager(64, 16)
+    bm.add_sequence(0, 70)  # 4 full blocks + 6 tokens
+    bm.fork(0, 1)
+    bm.fork(0, 2)
+    bm.add_sequence(3, 20)
+    assert bm.shared_prefix([0, 1, 2, 3], [0, 3, 4]).tolist() == [64, 0]
+    bm.append_token(1)  # private copy of the partial last block
+    assert bm.shared_prefix([0, 1, 2, 3], [0, 3, 4]).tolist() == [64, 0]
+    # sequences that share nothing, listed as one group
+    assert bm.shared_prefix([0, 3], [0, 2]).tolist() == [0]
+    # a group of one shares nothing
+    assert bm.shared_prefix([0, 1], [0, 1, 2]).tolist() == [0, 0]
+    # fill the shared partial block region in every member: still 4 blocks
+    # until the members' fifth blocks differ (after copy-on-write they do)
+    for _ in range(10):
+        for s in (0, 1, 2):
+            bm.append_token(s)
+    assert bm.shared_prefix([0, 1, 2], [0, 3]).tolist() == [64]
+    with pytest.raises(pagedkv.PagedKVError):
+        bm.shared_prefix([0, 99], [0, 2])  # unknown sequence
+    with pytest.raises(pagedkv.PagedKVError):
+        bm.shared_prefix([0, 1], [0, 1])  # groups do not cover the list

@@ -121,3 +121,77 @@ def test_copy_blocks_bit_exact_and_faults():
     ek[4] = ek[2]
     ev[4] = ev[2]
     assert torch.equal(k.cpu().view(torch.int16), ek.view(torch.int16))  # block 6 untouched
+
+
+def test_manager_driven_shared_prefix_decode_loop():
+    """Parallel sampling through the block manager: prompts forked into
+    families, every member grows by a token per step (copy-on-write of the
+    shared partial block), and each step decodes with the shared-prefix path,
+    its group description derived by the manager from the tables."""
+    D, H, Hkv, BS, NB, MB = 128, 16, 4, 16, 256, 40
+    tdt = torch.bfloat16
+    gen = torch.Generator().manual_seed(99)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen).to(tdt)  # noqa: E731
+    k_dev = torch.empty(NB, Hkv, BS, D, dtype=tdt, device="cuda")
+    v_dev = torch.empty_like(k_dev)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pool = pagedkv.BlockPool(k_dev, v_dev, err, zero_fill=True)
+    k_host = torch.zeros(NB, Hkv, BS, D, dtype=tdt)
+    v_host = torch.zeros_like(k_host)
+    bm = pagedkv.BlockManager(NB, BS)
+    scale = D ** -0.5
+
+    def write(slots, n):
+        keys, values = rnd(n, Hkv, D), rnd(n, Hkv, D)
+        sm = np.asarray(slots, dtype=np.int64)
+        assert oracle.reshape_and_cache(k_host, v_host, keys, values, sm) == 0
+        pagedkv.reshape_and_cache(pool, keys.cuda(), values.cuda(), torch.from_numpy(sm).cuda())
+
+    def copies():
+        src, dst = bm.take_copies()
+        if src.size:
+            k_host[torch.from_numpy(dst).long()] = k_host[torch.from_numpy(src).long()]
+            v_host[torch.from_numpy(dst).long()] = v_host[torch.from_numpy(src).long()]
+            pagedkv.copy_blocks(pool, torch.from_numpy(src).cuda(), torch.from_numpy(dst).cuda())
+
+    families = []  # lists of sequence ids, the prompt first
+    next_id = 0
+    for prompt, members in ((150, 4), (83, 3), (40, 1), (260, 2)):
+        write(bm.add_sequence(next_id, prompt), prompt)
+        fam = [next_id]
+        next_id += 1
+        for _ in range(members - 1):
+            bm.fork(fam[0], next_id)
+            fam.append(next_id)
+            next_id += 1
+        families.append(fam)
+
+    bt_dev = torch.empty(16, MB, dtype=torch.int32, device="cuda")
+    shared_seen = 0
+    for step in range(12):
+        live = [s for fam in families for s in fam]
+        gs = np.cumsum([0] + [len(f) for f in families]).astype(np.int32)
+        slots = [bm.append_token(s) for s in live]
+        copies()
+        write(slots, len(live))
+        bt_host, cl = bm.block_tables(live, MB)
+        prefix = bm.shared_prefix(live, gs)
+        shared_seen += int((prefix > 0).sum())
+        S = len(live)
+        pagedkv.block_table_upload(bt_dev[:S], torch.from_numpy(bt_host).pin_memory(), NB)
+        q = rnd(S, H, D)
+        out = torch.empty(S, H, D, dtype=torch.float32, device="cuda")
+        max_ctx, max_pre = int(cl.max()), int(prefix.max())
+        ws = torch.empty(pagedkv.shared_prefix_workspace_bytes(S, H, D, max_ctx, max_pre),
+                         dtype=torch.uint8, device="cuda")
+        pagedkv.paged_attention_decode_shared_prefix(
+            pool, out, q.cuda(), bt_dev[:S], torch.from_numpy(cl).cuda(), max_ctx, scale,
+            torch.from_numpy(gs).cuda(), torch.from_numpy(prefix).cuda(), max_pre, ws)
+        torch.cuda.synchronize()
+        assert pagedkv.get_device_error(pool) == 0
+        ref = oracle.paged_decode(q, k_host, v_host, bt_host, cl, scale)
+        assert_close(out, ref, "bf16", f"step {step}")
+        if step == 6:  # one family member finishes
+            bm.free_sequence(families[0].pop())
+    assert shared_seen >= 3 * 12  # three families shared blocks every step
+    assert torch.equal(k_dev.cpu().view(torch.int16), k_host.view(torch.int16))
