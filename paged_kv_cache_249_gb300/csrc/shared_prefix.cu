@@ -81,6 +81,7 @@ struct SpPlan {
     int max_prefix_len;     // tokens (already capped by max_context_len)
     int block_size;
     int pbp, pbs;           // blocks per prefix / suffix item
+    int cls_shift_p, cls_shift_s;  // size classes: (pbp - nb) >> cls_shift_p, likewise suffix
     int members_per_item;   // floor(32 / group)
     int num_heads, num_kv_heads, slots;  // recorded in the header for the run's check
     int prefix_cap;         // entries [0, prefix_cap) hold prefix items
@@ -89,78 +90,62 @@ struct SpPlan {
 
 __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
 
-// Exclusive block-wide scan of two counters (blockDim.x == kPlanThreads).
-__device__ void scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
-    __shared__ int wa[32], wb[32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int ia = a, ib = b;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int xa = __shfl_up_sync(0xffffffffu, ia, off);
-        const int xb = __shfl_up_sync(0xffffffffu, ib, off);
-        if (lane >= off) {
-            ia += xa;
-            ib += xb;
-        }
-    }
-    if (lane == 31) {
-        wa[warp] = ia;
-        wb[warp] = ib;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int va = wa[lane], vb = wb[lane];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int xa = __shfl_up_sync(0xffffffffu, va, off);
-            const int xb = __shfl_up_sync(0xffffffffu, vb, off);
-            if (lane >= off) {
-                va += xa;
-                vb += xb;
-            }
-        }
-        wa[lane] = va;
-        wb[lane] = vb;
-    }
-    __syncthreads();
-    const int pa = warp > 0 ? wa[warp - 1] : 0, pb = warp > 0 ? wb[warp - 1] : 0;
-    ea = pa + ia - a;
-    eb = pb + ib - b;
-    ta = wa[31];
-    tb = wb[31];
-    __syncthreads();  // wa/wb are reused by the next call
-}
-
-// One CTA turns the group description into the work list in one pass over
-// the groups: for every group with a shared prefix, ceil(members /
-// members_per_item) x ceil(prefix blocks / pbp) prefix items; for every
-// sequence, ceil(own blocks / pbs) suffix items.  Prefix items (the largest)
-// and suffix items go to separate regions; the decode kernel takes all
-// prefix items first, so its dynamic schedule ends on small items.  Context
-// lengths are staged in shared memory first (one parallel round trip), so
-// the per-group loops over members touch no global memory.
+// Items are listed largest first within each region (longest-processing-time
+// order): the persistent decode grid pulls them in list order, so its last
+// items are the shortest and its warps finish close together.  An item of nb
+// of at most cap blocks falls in size class (cap - nb) >> shift, with shift
+// the least that keeps classes below kPlanClasses (0 for cap <= 64: one class
+// per size).  The order inside a class is not fixed, and nothing depends on
+// it: every item writes its own partial slot.
+constexpr int kPlanClasses = 64;
 constexpr int kPlanSmemSeqs = 8192;
 
+// One CTA turns the group description into the work list.  A group with a
+// shared prefix gets ceil(members / members_per_item) x ceil(prefix blocks /
+// pbp) prefix items; every sequence gets ceil(own blocks / pbs) suffix items.
+// Prefix items (the largest) and suffix items go to separate regions, and the
+// decode kernel takes all prefix items first.  The first pass over the groups
+// checks each description and counts the items of every size class; after a
+// scan of the class counts, the second pass writes each item at the next
+// free entry of its class.  All inputs are read in one parallel round trip
+// (context lengths into shared memory, a thread's own group into registers),
+// so the passes touch no global memory but the work list.
 __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(const SpPlan p) {
     __shared__ int s_ctx[kPlanSmemSeqs];
+    __shared__ int s_cls[2][kPlanClasses];  // items per class, then the next free entry
+    __shared__ int s_tot[2];
     // the decode kernel may start setting up; it waits for this grid in
     // griddepcontrol.wait before it reads anything written here
     griddep_launch();
     griddep_wait();  // inputs written by the kernel before this one are complete
     const int tid = threadIdx.x;
+    if (tid < 2 * kPlanClasses) (&s_cls[0][0])[tid] = 0;
     const bool staged = p.num_seqs <= kPlanSmemSeqs;
     bool bad = false;
-    for (int i = tid; i <= p.num_groups; i += blockDim.x) {
-        const int v = __ldg(p.group_starts + i);
-        if (v < 0 || v > p.num_seqs) bad = true;
-        if (i == 0 && v != 0) bad = true;
-        if (i == p.num_groups && v != p.num_seqs) bad = true;
-        if (i < p.num_groups && v > __ldg(p.group_starts + i + 1)) bad = true;
-    }
-    for (int s = tid; s < p.num_seqs; s += blockDim.x) {
-        const int c = __ldg(p.context_lens + s);
-        if (c < 0 || c > p.ctx_cap) raise_fault(p.dev_error, PKV_FAULT_CONTEXT);
-        if (staged) s_ctx[s] = clamp_ctx(c, p.ctx_cap);
+    int my_start = 0, my_end = 0, my_plen = 0;  // group tid (when tid < num_groups)
+    for (int i = tid; i <= p.num_groups || i < p.num_seqs; i += blockDim.x) {
+        int v = 0, vn = 0, pl = 0, c = 0;
+        if (i <= p.num_groups) v = __ldg(p.group_starts + i);
+        if (i < p.num_groups) {
+            vn = __ldg(p.group_starts + i + 1);
+            pl = __ldg(p.prefix_lens + i);
+        }
+        if (i < p.num_seqs) c = __ldg(p.context_lens + i);
+        if (i <= p.num_groups) {
+            if (v < 0 || v > p.num_seqs) bad = true;
+            if (i == 0 && v != 0) bad = true;
+            if (i == p.num_groups && v != p.num_seqs) bad = true;
+            if (i < p.num_groups && v > vn) bad = true;
+        }
+        if (i < p.num_seqs) {
+            if (c < 0 || c > p.ctx_cap) raise_fault(p.dev_error, PKV_FAULT_CONTEXT);
+            if (staged) s_ctx[i] = clamp_ctx(c, p.ctx_cap);
+        }
+        if (i == tid) {
+            my_start = v;
+            my_end = vn;
+            my_plen = pl;
+        }
     }
     const bool flat = __syncthreads_or(bad);
     if (flat && tid == 0) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
@@ -170,74 +155,122 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     const int ngr = flat ? p.num_seqs : p.num_groups;
     const int BS = p.block_size, mpi = p.members_per_item;
 
-    int run_pre = 0, run_suf = 0;
+    // members [start, end) of group i and the blocks they share (0 = none);
+    // a description that breaks the rules shares nothing (and is reported)
+    auto group_of = [&](int i, int &start, int &end) -> int {
+        if (flat) {
+            start = i;
+            end = i + 1;
+            return 0;
+        }
+        int plen;
+        if (i == tid) {
+            start = my_start;
+            end = my_end;
+            plen = my_plen;
+        } else {
+            start = __ldg(p.group_starts + i);
+            end = __ldg(p.group_starts + i + 1);
+            plen = __ldg(p.prefix_lens + i);
+        }
+        if (plen == 0) return 0;
+        bool ok = plen > 0 && plen % BS == 0 && plen <= p.max_prefix_len;
+        for (int s = start; ok && s < end; ++s) ok = plen <= ctx_of(s);
+        if (!ok) {
+            raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+            return 0;
+        }
+        return end - start >= 2 ? plen / BS : 0;  // one member: nothing to share
+    };
+    auto cls_p = [&](int nb) { return (p.pbp - nb) >> p.cls_shift_p; };
+    auto cls_s = [&](int nb) { return (p.pbs - nb) >> p.cls_shift_s; };
+
+    // pass 1: items per size class
+    int my_pblk = 0;  // group tid's shared blocks, for pass 2
 #pragma unroll 1
-    for (int base = 0; base < ngr; base += blockDim.x) {
-        const int i = base + tid;
-        int start = 0, end = 0, pblk = 0, npre = 0, nsuf = 0, pp = 0;
-        if (i < ngr) {
-            // members [start, end) and the blocks they share (0 = none)
-            if (flat) {
-                start = i;
-                end = i + 1;
-            } else {
-                start = __ldg(p.group_starts + i);
-                end = __ldg(p.group_starts + i + 1);
-                const int plen = __ldg(p.prefix_lens + i);
-                if (plen != 0) {
-                    bool ok = plen > 0 && plen % BS == 0 && plen <= p.max_prefix_len;
-                    for (int s = start; ok && s < end; ++s) ok = plen <= ctx_of(s);
-                    if (!ok)
-                        raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-                    else if (end - start >= 2)  // one member: nothing to share
-                        pblk = plen / BS;
+    for (int i = tid; i < ngr; i += blockDim.x) {
+        int start, end;
+        const int pblk = group_of(i, start, end);
+        if (i == tid) my_pblk = pblk;
+        if (pblk > 0) {
+            const int pp = (pblk + p.pbp - 1) / p.pbp;
+            const int sets = (end - start + mpi - 1) / mpi;
+            if (pp > 1) atomicAdd(&s_cls[0][0], sets * (pp - 1));
+            atomicAdd(&s_cls[0][cls_p(pblk - (pp - 1) * p.pbp)], sets);
+        }
+        int full = 0;
+        for (int s = start; s < end; ++s) {
+            const int own = (ctx_of(s) + BS - 1) / BS - pblk;
+            if (own <= 0) continue;
+            const int nq = (own + p.pbs - 1) / p.pbs;
+            full += nq - 1;
+            atomicAdd(&s_cls[1][cls_s(own - (nq - 1) * p.pbs)], 1);
+        }
+        if (full > 0) atomicAdd(&s_cls[1][0], full);
+    }
+    __syncthreads();
+    // exclusive scan of the class counts: warp r for region r
+    if (tid < 64) {
+        const int r = tid >> 5, lane = tid & 31;
+        const int c0 = s_cls[r][2 * lane], c1 = s_cls[r][2 * lane + 1];
+        int inc = c0 + c1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += x;
+        }
+        const int ex = inc - c0 - c1;
+        s_cls[r][2 * lane] = ex;
+        s_cls[r][2 * lane + 1] = ex + c0;
+        if (lane == 31) s_tot[r] = inc;
+    }
+    __syncthreads();
+
+    // pass 2: every item at the next free entry of its class
+#pragma unroll 1
+    for (int i = tid; i < ngr; i += blockDim.x) {
+        int start, end, pblk;
+        if (i == tid) {
+            pblk = my_pblk;
+            start = flat ? i : my_start;
+            end = flat ? i + 1 : my_end;
+        } else {
+            pblk = group_of(i, start, end);
+        }
+        const int pp = (pblk + p.pbp - 1) / p.pbp;
+        for (int m0 = start; m0 < end && pp > 0; m0 += mpi) {
+            const int nm = min(mpi, end - m0);
+            for (int q = 0; q < pp; ++q) {
+                const int b0 = q * p.pbp, b1 = min(pblk, b0 + p.pbp);
+                const int e = atomicAdd(&s_cls[0][cls_p(b1 - b0)], 1);
+                if (e >= p.prefix_cap) {
+                    raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                    continue;
                 }
-            }
-            pp = (pblk + p.pbp - 1) / p.pbp;
-            npre = pp * ((end - start + mpi - 1) / mpi);
-            for (int s = start; s < end; ++s) {
-                const int nb = (ctx_of(s) + BS - 1) / BS;
-                nsuf += (nb - pblk + p.pbs - 1) / p.pbs;
+                p.entries[e] = SpEntry{m0, nm, start, b0, b1, q, b1 * BS, 0};
             }
         }
-        int ep, es, tp, ts;
-        scan2(npre, nsuf, ep, es, tp, ts);
-        if (i < ngr) {
-            int e = run_pre + ep;
-            for (int m0 = start; m0 < end && pp > 0; m0 += mpi) {
-                const int nm = min(mpi, end - m0);
-                for (int q = 0; q < pp; ++q, ++e) {
-                    if (e >= p.prefix_cap) {
-                        raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-                        continue;
-                    }
-                    const int b0 = q * p.pbp, b1 = min(pblk, b0 + p.pbp);
-                    p.entries[e] = SpEntry{m0, nm, start, b0, b1, q, b1 * BS, 0};
+        for (int s = start; s < end; ++s) {
+            const int ctx = ctx_of(s);
+            const int nb = (ctx + BS - 1) / BS;
+            int nq = 0;
+            for (int b0 = pblk; b0 < nb; b0 += p.pbs, ++nq) {
+                const int b1 = min(nb, b0 + p.pbs);
+                const int f = atomicAdd(&s_cls[1][cls_s(b1 - b0)], 1);
+                if (f >= p.suffix_cap) {
+                    raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+                    continue;
                 }
+                p.entries[p.prefix_cap + f] = SpEntry{s, 1, s, b0, b1, pp + nq, ctx, 0};
             }
-            int f = run_suf + es;
-            for (int s = start; s < end; ++s) {
-                const int ctx = ctx_of(s);
-                const int nb = (ctx + BS - 1) / BS;
-                int nq = 0;
-                for (int b0 = pblk; b0 < nb; b0 += p.pbs, ++nq, ++f) {
-                    if (f >= p.suffix_cap) {
-                        raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-                        continue;
-                    }
-                    p.entries[p.prefix_cap + f] = SpEntry{s, 1, s, b0, min(nb, b0 + p.pbs), pp + nq, ctx, 0};
-                }
-                p.nparts[s] = pp + nq;
-                p.share[2 * s] = start;
-                p.share[2 * s + 1] = pblk;
-            }
+            p.nparts[s] = pp + nq;
+            p.share[2 * s] = start;
+            p.share[2 * s + 1] = pblk;
         }
-        run_pre += tp;
-        run_suf += ts;
     }
     if (tid == 0) {
-        p.header[0] = run_pre < p.prefix_cap ? run_pre : p.prefix_cap;
-        p.header[1] = run_suf < p.suffix_cap ? run_suf : p.suffix_cap;
+        p.header[0] = s_tot[0] < p.prefix_cap ? s_tot[0] : p.prefix_cap;
+        p.header[1] = s_tot[1] < p.suffix_cap ? s_tot[1] : p.suffix_cap;
         p.header[2] = 0;  // work counter (the combine resets it after each run)
         // the geometry this plan was made for; a run checks it
         p.header[kSpHdrMagic] = kSpPlanMagic;
@@ -410,6 +443,14 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
                         : ((c.maxp + c.BS - 1) / c.BS > 0 ? (c.maxp + c.BS - 1) / c.BS : 1);
     p.pbs = c.z.pts > 0 ? c.z.pts / c.BS : (c.cap_blocks > 0 ? c.cap_blocks : 1);
     p.members_per_item = kSpRowsMax / c.group;
+    // least shift with (cap - 1) >> shift < kPlanClasses
+    auto cls_shift = [](int cap) {
+        int sh = 0;
+        while (((cap - 1) >> sh) >= kPlanClasses) ++sh;
+        return sh;
+    };
+    p.cls_shift_p = cls_shift(p.pbp);
+    p.cls_shift_s = cls_shift(p.pbs);
     p.prefix_cap = num_seqs * c.z.pp;
     p.suffix_cap = num_seqs * c.z.ps;
     return cuda_status(launch_dependent(shared_prefix_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, p));
