@@ -47,7 +47,7 @@ NCU_TRAFFIC: dict = {
     ("long_ctx", "plain"): {"bytes": 2975526000 + 48092416, "src": "57b8efbe4f5d189d"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
-    ("shared_prefix", "shared"): {"bytes": 856307456 + 40159488, "src": "77a7b37ebe8fe52e"},
+    ("shared_prefix", "shared"): {"bytes": 857671424 + 39637760, "src": "01d578879c1d426e"},
 }
 
 

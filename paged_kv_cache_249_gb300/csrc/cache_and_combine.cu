@@ -105,8 +105,8 @@ pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const in
 // partial outputs o_p and their log2-sum-exp lse_p.  The full softmax result
 // is sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M) with M = max_p lse_p,
 // which is exact: the partitions' exponentials share one max-free total.
-// One CTA per (sequence, head); two kernels, chosen on the host by the
-// number of partitions of the longest allowed context.
+// Two kernels, chosen on the host by the number of partitions of the
+// longest allowed context.
 constexpr int kCombThreads = 128;
 constexpr int kCombChunk = 1024;
 constexpr int kCombDirect = 16;  // up to this many partitions, the direct loop is faster
@@ -153,25 +153,60 @@ __device__ __forceinline__ void comb_store(const DecodeArgs &a, size_t oi, float
         reinterpret_cast<float *>(a.out)[oi] = res;
 }
 
-// Few partitions: each thread walks its column's parts directly.
-__global__ void __launch_bounds__(kCombThreads)
-    lse_combine_kernel(const DecodeArgs a, int head_dim, int block_size) {
-    __shared__ float red[kCombThreads / 32];
+// Few partitions: one warp per (sequence, head), each lane owning D/32
+// adjacent columns.  Every load the row needs (its context length, the
+// log2-sum-exps and partial outputs of all kCombDirect possible parts) is
+// issued before any is used, so the row costs one round trip to memory;
+// parts past the sequence's own count are loaded but never used.
+template <int PER>
+__global__ void __launch_bounds__(256)
+    lse_combine_kernel(const DecodeArgs a, int block_size, int rows) {
+    constexpr int D = PER * 32;
     griddep_wait();  // the decode grid's partials are complete
-    const CombRow r = comb_row(a, head_dim, block_size, blockIdx.x);
-    if (r.nparts <= 1) return;  // the decode kernel wrote this row directly
-    const float M = comb_max(r, red);
-    for (int d = threadIdx.x; d < head_dim; d += kCombThreads) {
-        float num = 0.f, den = 0.f;
-        if (M != -CUDART_INF_F) {
-            for (int p = 0; p < r.nparts; ++p) {
-                const float w = fast_exp2(r.lse[p] - M);
-                den += w;
-                num = fmaf(w, r.po[(size_t)p * head_dim + d], num);
+    const int sh = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (sh >= rows) return;
+    const int P = a.num_parts;  // <= kCombDirect
+    int ctx = __ldg(a.context_lens + sh / a.num_heads);
+    const float lse_l = lane < P ? a.ws_lse[(size_t)sh * P + lane] : -CUDART_INF_F;
+    const float *po = a.ws_o + (size_t)sh * P * D + lane * PER;
+    float v[kCombDirect][PER];
+#pragma unroll
+    for (int p = 0; p < kCombDirect; ++p) {
+        if (p < P) {
+            if constexpr (PER == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(po + (size_t)p * D);
+                v[p][0] = x.x, v[p][1] = x.y, v[p][2] = x.z, v[p][3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(po + (size_t)p * D);
+                v[p][0] = x.x, v[p][1] = x.y;
             }
         }
-        comb_store(a, (size_t)r.sh * head_dim + d, den > 0.f ? num / den : 0.f);
     }
+    ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
+    const int nblk = (ctx + block_size - 1) / block_size;
+    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+    if (nparts <= 1) return;  // the decode kernel wrote this row directly
+    float M = lane < nparts ? lse_l : -CUDART_INF_F;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w_l = lane < nparts && M != -CUDART_INF_F ? fast_exp2(lse_l - M) : 0.f;
+    float den = w_l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    float num[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) num[j] = 0.f;
+#pragma unroll
+    for (int p = 0; p < kCombDirect; ++p) {
+        const float w = __shfl_sync(0xffffffffu, w_l, p);
+        if (p < nparts) {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) num[j] = fmaf(w, v[p][j], num[j]);
+        }
+    }
+    const size_t oi = (size_t)sh * D + lane * PER;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) comb_store(a, oi + j, den > 0.f ? num[j] / den : 0.f);
 }
 
 // Many partitions (a long context has hundreds): each (sequence, head) is
@@ -234,9 +269,14 @@ pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, i
                               cudaStream_t stream) {
     const long long n = (long long)num_seqs * a.num_heads;
     if (n == 0) return PKV_OK;
-    if (a.num_parts <= kCombDirect)
-        return cuda_status(launch_dependent(lse_combine_kernel, dim3((unsigned)n),
-                                            dim3(kCombThreads), 0, stream, a, head_dim, block_size));
+    if (a.num_parts <= kCombDirect) {
+        const dim3 grid((unsigned)((n + 7) / 8));
+        if (head_dim == 64)
+            return cuda_status(launch_dependent(lse_combine_kernel<2>, grid, dim3(256), 0, stream, a,
+                                                block_size, (int)n));
+        return cuda_status(launch_dependent(lse_combine_kernel<4>, grid, dim3(256), 0, stream, a,
+                                            block_size, (int)n));
+    }
     return cuda_status(launch_dependent(lse_combine_many_kernel,
                                         dim3((unsigned)(n * (head_dim / kCombCols))),
                                         dim3(kCombThreads), 0, stream, a, head_dim, block_size));

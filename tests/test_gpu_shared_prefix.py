@@ -209,3 +209,64 @@ def test_run_without_or_against_another_plan_is_reported():
     dw.sp_partition = -1  # a run with another geometry than the plan's (fits the workspace)
     dw.decode_shared_prefix_run()
     assert pagedkv.get_device_error(dw.pool) & pagedkv.FAULT_PREFIX
+
+
+# ------------------------------------------------------------ the work list
+
+def _expected_items(w, pbp, pbs):
+    """Work items of the group description, derived on the host: per group
+    with a shared prefix, ceil(members / floor(32 / G)) row sets x the prefix
+    parts; per sequence, its own blocks after the prefix in parts of pbs."""
+    BS, G = w.block_size, w.num_heads // w.num_kv_heads
+    mpi = 32 // G
+    gs, gp = w.groups()
+    ctx = np.asarray(w.context_lens)
+    pre, suf = [], []
+    for i in range(len(gp)):
+        start, end = int(gs[i]), int(gs[i + 1])
+        pblk = int(gp[i]) // BS if end - start >= 2 else 0
+        pp = -(-pblk // pbp)
+        for m0 in range(start, end, mpi):
+            for q in range(pp):
+                b0, b1 = q * pbp, min(pblk, (q + 1) * pbp)
+                pre.append((m0, min(mpi, end - m0), start, b0, b1, q, b1 * BS))
+        for s in range(start, end):
+            nb = -(-int(ctx[s]) // BS)
+            for k, b0 in enumerate(range(pblk, nb, pbs)):
+                suf.append((s, 1, s, b0, min(nb, b0 + pbs), pp + k, int(ctx[s])))
+    return pre, suf
+
+
+@pytest.mark.parametrize("case", ["g4_ragged_groups", "big_group", "g3_odd"])
+def test_plan_lists_every_item_once_largest_first(case):
+    """The plan's entries are exactly the items of the description, each
+    region (prefix items, then suffix items) in non-increasing block count, so
+    the persistent grid's last items are its shortest."""
+    ctx, groups, H, Hkv, D, BS = CASES[case]
+    w = _w(case, ctx, groups, H, Hkv, D, BS, seed=31)
+    dw = pagedkv.DeviceWorkload(w)
+    dw.shared_prefix_setup(partition_tokens=64)
+    dw.shared_prefix_plan()
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw.pool) == 0
+    ws = dw.sp_workspace.cpu().numpy().view(np.int32)
+    S = w.num_seqs
+    r = lambda x: -(-x // 256) * 256  # noqa: E731
+    off_entries = (256 + r(S * 4) + r(S * 8)) // 4
+    pbp = pbs = 64 // BS
+    pp = -(-min(dw.max_prefix_len, dw.max_context_len) // 64)
+    n_pre, n_suf = int(ws[0]), int(ws[1])
+    ent = ws[off_entries:].reshape(-1, 8)
+    got_pre = [tuple(int(x) for x in e[:7]) for e in ent[:n_pre]]
+    got_suf = [tuple(int(x) for x in e[:7]) for e in ent[S * pp:S * pp + n_suf]]
+    exp_pre, exp_suf = _expected_items(w, pbp, pbs)
+    assert sorted(got_pre) == sorted(exp_pre)
+    assert sorted(got_suf) == sorted(exp_suf)
+    for got in (got_pre, got_suf):
+        sizes = [e[4] - e[3] for e in got]
+        assert sizes == sorted(sizes, reverse=True), sizes
+    # partial counts: prefix parts plus own parts of every sequence
+    nparts = ws[64:64 + S]
+    for s in range(S):
+        assert nparts[s] == sum(1 for e in exp_pre if e[0] <= s < e[0] + e[1]) + \
+            sum(1 for e in exp_suf if e[0] == s)
