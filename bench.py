@@ -327,6 +327,15 @@ def run_native(args, world: int, rank: int) -> dict | None:
     barrier(world)
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    # the cache write alone (reported beside the decode, outside the timed step)
+    ev_rc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(min(args.steps, 200))]
+    for a_, b_ in ev_rc:
+        a_.record(stream)
+        pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    rc_us = float(np.median([a_.elapsed_time(b_) for a_, b_ in ev_rc])) * 1e3
     clock_info = clocks.stop() if clocks else None
     fault = pagedkv.get_device_error(dw.pool)
     if fault:
@@ -497,6 +506,12 @@ def run_native(args, world: int, rank: int) -> dict | None:
         "config": workload_config(w, args.workload, world),
         "seqs_per_s": round(seqs_per_s, 1),
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
+        # reported beside the KV bytes: the decode call's other traffic, the
+        # cache write's time, and sequences per second of the decode call alone
+        "side": {"q_bytes": ab["q"], "out_bytes": ab["out"], "block_table_bytes": ab["table"],
+                 "context_len_bytes": w.num_seqs * 4, "new_kv_bytes": ab["new_kv"],
+                 "reshape_and_cache_us": round(rc_us, 2),
+                 "seqs_per_s_decode_call": round(w.num_seqs / dec_avg_s, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
