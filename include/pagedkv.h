@@ -5,8 +5,8 @@
  * The operations follow the PagedAttention pages:
  *   - the KV cache is cut into fixed-size blocks that need not be contiguous
  *     in device memory (Qualiteg, "About PagedAttention for LLM serving",
- *     section "1-2 ... divides the KV cache into blocks"; block sizes of
- *     "around 16 to 256" are suggested there);
+ *     section "1-2 ... divides the KV cache into blocks", which suggests blocks
+ *     of roughly 16 to 256 tokens);
  *   - logical blocks of a sequence map onto physical blocks through a block
  *     table (same page, section "There are logical blocks and physical
  *     blocks, and the two are linked by a block table");
