@@ -102,8 +102,10 @@ size_t pkv_pool_bytes(int num_blocks, int block_size, int num_kv_heads, int head
  * k_pool/v_pool: device buffers of pkv_pool_bytes(...) bytes each, on the
  * current device.  dev_error: device int32 error word or NULL.  zero_fill:
  * non-zero clears both pools and the error word on `stream`.
- * Supported: block_size in {16, 32}; head_dim in {64, 128}; dtype F32 or
- * BF16; num_blocks*num_kv_heads*block_size < 2^31.
+ * Supported: block_size in {16, 32, 64, 128, 256} (the page's range of
+ * roughly 16 to 256 tokens; blocks above 32 tokens are staged in runs of 32
+ * rows); head_dim in {64, 128}; dtype F32 or BF16;
+ * num_blocks*num_kv_heads*block_size < 2^31.
  */
 pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, int num_kv_heads,
                                int head_dim, pkv_dtype dtype, void *k_pool, void *v_pool,
@@ -269,7 +271,8 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: bf16 pools,
- * num_heads / num_kv_heads in 1..16, out_dtype F32 or BF16.
+ * num_heads / num_kv_heads in 1..16, block_size 16 or 32, out_dtype F32 or
+ * BF16.
  */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_context_len, int max_prefix_len,

@@ -33,8 +33,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Rows of one staged run of a block: the whole block up to kMaxStageRows;
+// a larger block (64, 128 or 256 rows) is staged in runs of kMaxStageRows.
+int stage_rows(int block_size) { return block_size < kMaxStageRows ? block_size : kMaxStageRows; }
+
 // Descriptor of one pool seen as a 2-D tensor [rows = NB*Hkv*BS][head_dim],
-// staged in boxes of one 128-byte slab x block_size rows with the 128-byte
+// staged in boxes of one 128-byte slab x one run of rows with the 128-byte
 // swizzle the kernels read back.
 bool encode_pool_map(CUtensorMap *map, void *base, int rows, int head_dim, int block_size,
                      pkv_dtype dtype) {
@@ -43,7 +47,7 @@ bool encode_pool_map(CUtensorMap *map, void *base, int rows, int head_dim, int b
     const int elem = dtype == PKV_BF16 ? 2 : 4;
     const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)head_dim * elem};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)block_size};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)stage_rows(block_size)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
@@ -61,7 +65,9 @@ static_assert(sizeof(((pkv_pool *)nullptr)->tma) == 256, "pool descriptor storag
 
 bool valid_geometry(int num_blocks, int block_size, int num_kv_heads, int head_dim) {
     if (num_blocks <= 0 || num_kv_heads <= 0) return false;
-    if (block_size != 16 && block_size != 32) return false;
+    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 &&
+        block_size != 256)
+        return false;
     if (head_dim != 64 && head_dim != 128) return false;
     return (long long)num_blocks * num_kv_heads * block_size < (1ll << 31);
 }
@@ -262,10 +268,15 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
     if (dev != pool->device) return PKV_ERR_INVALID_ARG;
 
-    const int BS = pool->block_size;
+    // The kernel works in staged runs of U rows: a block of BS > 32 rows is
+    // 2^unit_shift runs, and partitions (whole blocks) are whole runs.
+    const int BS = pool->block_size, U = stage_rows(BS);
+    int unit_shift = 0;
+    while ((U << unit_shift) < BS) ++unit_shift;
+    if (((long long)max_blocks_per_seq << unit_shift) >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
     const long long table_cap = (long long)max_blocks_per_seq * BS;
     const int ctx_cap = (int)(table_cap < max_context_len ? table_cap : max_context_len);
-    const int cap_blocks = (ctx_cap + BS - 1) / BS;
+    const int cap_blocks = (ctx_cap + U - 1) / U;  // runs
 
     DecodeArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -282,13 +293,14 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     a.ctx_cap = ctx_cap;
     a.out_bf16 = out_dtype == PKV_BF16;
     a.contig = contig ? 1 : 0;
+    a.unit_shift = unit_shift;
     a.scale_log2 = scale * 1.4426950408889634f;
 
     const int pt = resolve_partition(partition_tokens, ctx_cap, (long long)num_seqs * num_kv_heads,
                                      sm_count(dev));
     int parts = 1;
     if (pt > 0) {
-        a.part_blocks = pt / BS;
+        a.part_blocks = pt / U;
         parts = (cap_blocks + a.part_blocks - 1) / a.part_blocks;
         if (parts < 1) parts = 1;
     }
@@ -315,7 +327,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     L.args = a;
     L.num_seqs = num_seqs;
     L.head_dim = pool->head_dim;
-    L.block_size = BS;
+    L.block_size = U;
     int gp = 1;
     while (gp < group) gp <<= 1;
     L.group_pad = gp;
@@ -329,7 +341,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     else
         st = pool->head_dim == 64 ? launch_decode_f32_d64(L) : launch_decode_f32_d128(L);
     if (st != PKV_OK || parts <= 1) return st;
-    return launch_lse_combine(a, num_seqs, pool->head_dim, BS, L.stream);
+    return launch_lse_combine(a, num_seqs, pool->head_dim, U, L.stream);
 }
 
 pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype out_dtype,

@@ -468,14 +468,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     // Gather this warp's first block numbers before the context length is
     // known (bounded by the table row), so the two dependent loads overlap.
+    // (Blocks here are staged runs of BS rows: a pool block of more than 32
+    // rows is 2^ushift runs, all named by its one table entry.  Only the
+    // 32-row instantiation stages such blocks.)
+    const int ushift = BS == kMaxStageRows ? a.unit_shift : 0;
     const int b0 = part * a.part_blocks;
-    const int tspan = min(a.max_blocks_per_seq, b0 + a.part_blocks) - b0;
+    const int tspan = min(a.max_blocks_per_seq << ushift, b0 + a.part_blocks) - b0;
     const int nw_tbl = tspan > warp ? (tspan - warp + NW - 1) / NW : 0;
     const int32_t *bt_row = a.block_tables + (size_t)s * a.max_blocks_per_seq;
     auto bt_load = [&](int chunk) -> int {
         const int i = chunk * 32 + lane;
         if (i >= nw_tbl) return -1;
-        return a.contig ? b0 + warp + i * NW : __ldg(bt_row + b0 + warp + i * NW);
+        return a.contig ? b0 + warp + i * NW : __ldg(bt_row + ((b0 + warp + i * NW) >> ushift));
     };
     int ent0 = bt_load(0), ent1 = bt_load(1);
 
@@ -516,8 +520,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                 mbar_arrive_expect_tx(bar, Gm::kStageBytes);
                 unsigned char *dk = wstage + (i % NST) * Gm::kStageBytes;
                 unsigned char *dv = dk + Gm::kTileBytes;
+                const int run = (b0 + warp + i * NW) & ((1 << ushift) - 1);
                 const int y = a.contig ? ((s * a.num_kv_heads + g) * a.num_blocks + pb) * BS
-                                       : (pb * a.num_kv_heads + g) * BS;
+                                       : (((pb * a.num_kv_heads + g) << ushift) + run) * BS;
 #pragma unroll
                 for (int sl = 0; sl < Gm::kSlabs; ++sl) {
                     tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);

@@ -14,6 +14,7 @@ constexpr uint32_t kPoolMagic = 0x504b5631u;  // "PKV1"
 constexpr int kAutoPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 8192;
 constexpr int kMaxGroup = 16;
+constexpr int kMaxStageRows = 32;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 
 // Arguments of one decode launch; every pointer is a device pointer.
@@ -35,6 +36,7 @@ struct DecodeArgs {
     int num_parts;              // gridDim.z: partitions of the longest allowed context
     int out_bf16;
     int contig;                 // 1: contiguous cache, block b of (s, g) is row run (s*Hkv+g)*num_blocks+b
+    int unit_shift;             // a pool block is 2^unit_shift staged runs of BS rows (blocks over 32 rows)
     float scale_log2;           // scale * log2(e)
 };
 

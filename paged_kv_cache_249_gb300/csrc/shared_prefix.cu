@@ -399,7 +399,7 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
         (partition_tokens > 0 && partition_tokens % c.BS != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (pool->dtype != PKV_BF16 || pool->block_size > kMaxStageRows) return PKV_ERR_UNSUPPORTED;
     c.group = num_heads / num_kv_heads;
     if (c.group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
     c.z = sp_sizes(partition_tokens, max_context_len, max_prefix_len);

@@ -130,7 +130,10 @@ def test_pool_init_and_cache_write_reject_bad_arguments(lib):
     init = lib.pkv_block_pool_init
     assert init(None, 8, 16, 2, 128, pagedkv.BF16, 0x1000, 0x2000, None, 0, None) == E
     assert init(ctypes.byref(p), 8, 16, 2, 128, pagedkv.BF16, 0, 0x2000, None, 0, None) == E
-    assert init(ctypes.byref(p), 8, 24, 2, 128, pagedkv.BF16, 0x1000, 0x2000, None, 0, None) == U
+    # block sizes: 16, 32, 64, 128 or 256 tokens (the page's range of roughly 16 to 256)
+    for bs in (8, 24, 48, 96, 512):
+        assert init(ctypes.byref(p), 8, bs, 2, 128, pagedkv.BF16, 0x1000, 0x2000, None, 0,
+                    None) == U, bs
     assert init(ctypes.byref(p), 8, 16, 2, 96, pagedkv.BF16, 0x1000, 0x2000, None, 0, None) == U
     assert init(ctypes.byref(p), 8, 16, 2, 128, 5, 0x1000, 0x2000, None, 0, None) == E
     assert init(ctypes.byref(p), 8, 16, 2, 128, pagedkv.BF16, 0x1008, 0x2000, None, 0, None) == E

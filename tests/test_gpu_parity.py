@@ -4,6 +4,8 @@ Cache writes are compared byte for byte over the whole pool; attention
 outputs within 1e-5 (fp32 inputs) or 2e-3 (bf16 inputs, fp32 accumulation),
 on sizes that span several tiles, partitions and a ragged last block.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -129,3 +131,81 @@ def test_random_shapes_sweep():
         dw = run_decode(w, partition_tokens=pt)
         assert pagedkv.get_device_error(dw.pool) == 0
         assert_close(dw.out, ref, dtype, f"trial {trial}: {dtype} D{D} BS{BS} G{G} ctx {ctx} pt {pt}")
+
+
+# ------------------------------------------------- blocks of 64 to 256 tokens
+
+LARGE_BLOCK_CASES = [
+    # dtype, D, BS, H, Hkv
+    ("bf16", 128, 64, 32, 8),
+    ("bf16", 128, 128, 8, 8),
+    ("bf16", 64, 256, 16, 2),
+    ("f32", 64, 64, 4, 4),
+    ("f32", 128, 256, 8, 2),
+]
+
+
+@pytest.mark.parametrize("case", LARGE_BLOCK_CASES, ids=lambda c: "_".join(map(str, c)))
+def test_large_blocks_match_oracle(case):
+    """Blocks of 64, 128 and 256 tokens (the page's range of roughly 16 to
+    256): the kernel stages each block in runs of 32 rows named by the
+    block's one table entry; contexts end mid-run, mid-block, on a run and on
+    a block boundary."""
+    dtype, D, BS, H, Hkv = case
+    ctx = [1, 31, 32, 33, BS - 1, BS, BS + 1, 3 * BS + 17, 1000]
+    w = _w(dtype, D, BS, H, Hkv, ctx=ctx, seed=400 + LARGE_BLOCK_CASES.index(case))
+    ref, _, _ = oracle_after_write(w)
+    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_FMA] + ([pagedkv.PATH_MMA] if dtype == "bf16" else [])
+    for pt in (-1, 0, 2 * BS):
+        for path in paths:
+            dw = run_decode(w, path=path, partition_tokens=pt)
+            assert pagedkv.get_device_error(dw.pool) == 0
+            assert_close(dw.out, ref, dtype, f"{case} path={path} partition={pt}")
+
+
+@pytest.mark.parametrize("BS", [64, 256])
+def test_large_block_cache_write_bit_exact(BS):
+    w = _w("bf16", 128, BS, 8, 4, ctx=[1, BS, BS + 1, 2 * BS + 5], seed=450)
+    dw = pagedkv.DeviceWorkload(w)
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw.pool) == 0
+    kp, vp = w.k_pool.clone(), w.v_pool.clone()
+    assert oracle.reshape_and_cache(kp, vp, w.new_key, w.new_value, w.slot_mapping) == 0
+    assert torch.equal(dw.k_pool.cpu().view(torch.int16), kp.view(torch.int16))
+    assert torch.equal(dw.v_pool.cpu().view(torch.int16), vp.view(torch.int16))
+
+
+def _reblock(w, BS):
+    """The same logical tokens laid out in blocks of BS (sequential placement)."""
+    S, Hkv, D = w.num_seqs, w.num_kv_heads, w.head_dim
+    nblk = [-(-int(c) // BS) for c in w.context_lens]
+    NB, MB = sum(nblk), max(nblk)
+    k = torch.zeros((NB, Hkv, BS, D), dtype=w.k_pool.dtype)
+    v = torch.zeros_like(k)
+    bt = np.full((S, MB), -1, dtype=np.int32)
+    nxt = 0
+    for s in range(S):
+        for b in range(nblk[s]):
+            bt[s, b] = nxt
+            for j in range(b * BS, min(int(w.context_lens[s]), (b + 1) * BS)):
+                ob, orow = int(w.block_tables[s, j // w.block_size]), j % w.block_size
+                k[nxt, :, j % BS] = w.k_pool[ob, :, orow]
+                v[nxt, :, j % BS] = w.v_pool[ob, :, orow]
+            nxt += 1
+    slot = np.array([int(bt[s, (int(c) - 1) // BS]) * BS + (int(c) - 1) % BS
+                     for s, c in enumerate(w.context_lens)], dtype=np.int64)
+    return dataclasses.replace(w, block_size=BS, num_blocks=NB, max_blocks_per_seq=MB,
+                               block_tables=bt, slot_mapping=slot, k_pool=k, v_pool=v)
+
+
+def test_large_blocks_equal_small_blocks_bitwise():
+    """The same tokens in blocks of 256 and of 32 give the same bits: the
+    kernel's arithmetic runs over 32-row runs either way, in the same order."""
+    w256 = _w("bf16", 128, 256, 32, 8, ctx=[5, 300, 777, 1024], seed=460)
+    outs = []
+    for w in (w256, _reblock(w256, 32)):
+        dw = run_decode(w, partition_tokens=512)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        outs.append(dw.out.cpu())
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
