@@ -42,9 +42,9 @@ FALLBACK_HBM_GBS = 6800.0
 # sources hash to `src`.  Filled in from the profiles summaries.
 NCU_TRAFFIC: dict = {
     # profiles/paged_decode_kernel_mha_7b_gqa_8b_long_ctx.md
-    ("mha_7b", "plain"): {"bytes": 1105862000 + 5882624, "src": "57b8efbe4f5d189d"},
-    ("gqa_8b", "plain"): {"bytes": 2374026000 + 13411840, "src": "57b8efbe4f5d189d"},
-    ("long_ctx", "plain"): {"bytes": 2975526000 + 48092416, "src": "57b8efbe4f5d189d"},
+    ("mha_7b", "plain"): {"bytes": 1105864000 + 5669632, "src": "8538972e68c679ea"},
+    ("gqa_8b", "plain"): {"bytes": 2374010000 + 13422848, "src": "8538972e68c679ea"},
+    ("long_ctx", "plain"): {"bytes": 2975505000 + 48528640, "src": "8538972e68c679ea"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
     ("shared_prefix", "shared"): {"bytes": 857671424 + 39637760, "src": "01d578879c1d426e"},
