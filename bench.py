@@ -47,7 +47,7 @@ NCU_TRAFFIC: dict = {
     ("long_ctx", "plain"): {"bytes": 2975505000 + 48528640, "src": "8538972e68c679ea"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
-    ("shared_prefix", "shared"): {"bytes": 857671424 + 39637760, "src": "01d578879c1d426e"},
+    ("shared_prefix", "shared"): {"bytes": 857698816 + 39856896, "src": "c064e8ad5ec2d359"},
 }
 
 
