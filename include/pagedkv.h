@@ -271,8 +271,7 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: bf16 pools,
- * num_heads / num_kv_heads in 1..16, block_size 16 or 32, out_dtype F32 or
- * BF16.
+ * num_heads / num_kv_heads in 1..16, out_dtype F32 or BF16.
  */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_context_len, int max_prefix_len,

@@ -83,7 +83,9 @@ struct SpArgs {
                                 // [kSpHdrMagic..] the plan's geometry (planning kernel)
     int suffix_base;
     int num_seqs;
-    int block_size;
+    int block_size;             // tokens per pool block
+    int unit_shift;             // a block is 2^unit_shift staged runs (blocks over 32 tokens);
+                                // work items count runs
     int num_heads;
     int num_kv_heads;
     int group;

@@ -79,7 +79,8 @@ struct SpPlan {
     int num_groups, num_seqs;
     int ctx_cap;            // context lengths are clamped to [0, ctx_cap]
     int max_prefix_len;     // tokens (already capped by max_context_len)
-    int block_size;
+    int block_size;         // tokens per pool block (a shared prefix is whole blocks)
+    int run_rows;           // tokens per staged run (min(block_size, 32)); the work list counts runs
     int pbp, pbs;           // blocks per prefix / suffix item
     int cls_shift_p, cls_shift_s;  // size classes: (pbp - nb) >> cls_shift_p, likewise suffix
     int members_per_item;   // floor(32 / group)
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         return staged ? s_ctx[s] : clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
     };
     const int ngr = flat ? p.num_seqs : p.num_groups;
-    const int BS = p.block_size, mpi = p.members_per_item;
+    const int BS = p.run_rows, mpi = p.members_per_item;
 
     // members [start, end) of group i and the blocks they share (0 = none);
     // a description that breaks the rules shares nothing (and is reported)
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
             plen = __ldg(p.prefix_lens + i);
         }
         if (plen == 0) return 0;
-        bool ok = plen > 0 && plen % BS == 0 && plen <= p.max_prefix_len;
+        bool ok = plen > 0 && plen % p.block_size == 0 && plen <= p.max_prefix_len;
         for (int s = start; ok && s < end; ++s) ok = plen <= ctx_of(s);
         if (!ok) {
             raise_fault(p.dev_error, PKV_FAULT_PREFIX);
@@ -301,7 +302,8 @@ __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs
     const int np = a.nparts[s];
     if (wid % a.num_heads == 0) {
         // members must name their leader's blocks inside the shared prefix
-        const int leader = a.seq_share[2 * s], pblk = a.seq_share[2 * s + 1];
+        // (the plan records shared runs; the table has one entry per block)
+        const int leader = a.seq_share[2 * s], pblk = a.seq_share[2 * s + 1] >> a.unit_shift;
         if (pblk > 0 && leader != s) {
             const int32_t *mine = a.block_tables_chk + (size_t)s * a.max_blocks_per_seq;
             const int32_t *lead = a.block_tables_chk + (size_t)leader * a.max_blocks_per_seq;
@@ -380,7 +382,7 @@ namespace {
 
 // Host-side checks and sizes shared by the plan, the run and the combined call.
 struct SpCall {
-    int BS, group, dev, ctx_cap, maxp, cap_blocks;
+    int BS, U, unit_shift, group, dev, ctx_cap, maxp, cap_blocks;  // cap_blocks counts runs of U
     SpSizes z;
     SpLayout lay;
 };
@@ -399,7 +401,12 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
         (partition_tokens > 0 && partition_tokens % c.BS != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    if (pool->dtype != PKV_BF16 || pool->block_size > kMaxStageRows) return PKV_ERR_UNSUPPORTED;
+    if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    // blocks above kMaxStageRows tokens are staged (and listed) in runs
+    c.U = c.BS < kMaxStageRows ? c.BS : kMaxStageRows;
+    c.unit_shift = 0;
+    while ((c.U << c.unit_shift) < c.BS) ++c.unit_shift;
+    if (((long long)max_blocks_per_seq << c.unit_shift) >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
     c.group = num_heads / num_kv_heads;
     if (c.group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
     c.z = sp_sizes(partition_tokens, max_context_len, max_prefix_len);
@@ -411,7 +418,7 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
     const long long table_cap = (long long)max_blocks_per_seq * c.BS;
     c.ctx_cap = (int)(table_cap < max_context_len ? table_cap : max_context_len);
     c.maxp = max_prefix_len < max_context_len ? max_prefix_len : max_context_len;
-    c.cap_blocks = (c.ctx_cap + c.BS - 1) / c.BS;
+    c.cap_blocks = (c.ctx_cap + c.U - 1) / c.U;
     if (cuda_status(cudaGetDevice(&c.dev)) != PKV_OK) return PKV_ERR_CUDA;
     if (c.dev != pool->device) return PKV_ERR_INVALID_ARG;
     return PKV_OK;
@@ -439,9 +446,10 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
     p.ctx_cap = c.ctx_cap;
     p.max_prefix_len = c.maxp;
     p.block_size = c.BS;
-    p.pbp = c.z.ptp > 0 ? c.z.ptp / c.BS
-                        : ((c.maxp + c.BS - 1) / c.BS > 0 ? (c.maxp + c.BS - 1) / c.BS : 1);
-    p.pbs = c.z.pts > 0 ? c.z.pts / c.BS : (c.cap_blocks > 0 ? c.cap_blocks : 1);
+    p.run_rows = c.U;
+    p.pbp = c.z.ptp > 0 ? c.z.ptp / c.U
+                        : ((c.maxp + c.U - 1) / c.U > 0 ? (c.maxp + c.U - 1) / c.U : 1);
+    p.pbs = c.z.pts > 0 ? c.z.pts / c.U : (c.cap_blocks > 0 ? c.cap_blocks : 1);
     p.members_per_item = kSpRowsMax / c.group;
     // least shift with (cap - 1) >> shift < kPlanClasses
     auto cls_shift = [](int cap) {
@@ -481,6 +489,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     a.num_kv_heads = pool->num_kv_heads;
     a.group = c.group;
     a.block_size = c.BS;
+    a.unit_shift = c.unit_shift;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = pool->num_blocks;
     a.num_slots = c.z.slots;
@@ -494,7 +503,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     L.tmv = &maps[1];
     L.args = a;
     L.head_dim = pool->head_dim;
-    L.block_size = c.BS;
+    L.block_size = c.U;
     L.stream = st;
     L.device = c.dev;
     const pkv_status s1 =

@@ -280,25 +280,27 @@ __global__ void __launch_bounds__(kSpWarps * 32)
         t.R = t.nseq * G;
         return t;
     };
-    // physical block of the item's i-th block (chunk of 32, one per lane)
+    // physical block of the item's i-th run (chunk of 32, one per lane); a
+    // block of more than 32 tokens is 2^ushift runs, named by one table entry
+    const int ushift = BS == kMaxStageRows ? a.unit_shift : 0;
     auto bt_load = [&](const SpItem &t, int chunk) -> int {
         const int i = chunk * 32 + lane;
         if (i >= t.nb) return -1;
-        return __ldg(a.block_tables + (size_t)t.tbl_seq * a.max_blocks_per_seq + t.b0 + i);
+        return __ldg(a.block_tables + (size_t)t.tbl_seq * a.max_blocks_per_seq + ((t.b0 + i) >> ushift));
     };
     // partial count of the sequence of row `lane` of the item
     auto nparts_of = [&](const SpItem &t) -> int {
         return lane < t.R ? a.nparts[t.seq0 + lane / G] : 0;
     };
-    // stage the item's block at absolute ring position k
-    auto issue = [&](int g, unsigned k, int pb) {
+    // stage run `run` (of its sequence) of block pb at absolute ring position k
+    auto issue = [&](int g, unsigned k, int pb, int run) {
         if (lane == 0) {
             uint64_t *bar = &wbar[k % NST];
             if (pb >= 0 && pb < a.num_blocks) {
                 mbar_arrive_expect_tx(bar, Gm::kStageBytes);
                 unsigned char *dk = wstage + (k % NST) * Gm::kStageBytes;
                 unsigned char *dv = dk + Gm::kTileBytes;
-                const int y = (pb * Hkv + g) * BS;
+                const int y = (((pb * Hkv + g) << ushift) + (run & ((1 << ushift) - 1))) * BS;
 #pragma unroll
                 for (int sl = 0; sl < Gm::kSlabs; ++sl) {
                     tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
         int np = nparts_of(it);
         int ent0 = bt_load(it, 0), ent1 = bt_load(it, 1);
 #pragma unroll 1
-        for (int j = 0; j < NST && j < it.nb; ++j) issue(it.g, j, __shfl_sync(FULL, ent0, j));
+        for (int j = 0; j < NST && j < it.nb; ++j) issue(it.g, j, __shfl_sync(FULL, ent0, j), it.b0 + j);
 #pragma unroll 1
         for (;;) {
             cp_async_wait_all();
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                                                            a.scale_log2, lane);
                 }
                 __syncwarp();
-                if (i + NST < it.nb) issue(it.g, kk + NST, bt_get(i + NST));
+                if (i + NST < it.nb) issue(it.g, kk + NST, bt_get(i + NST), it.b0 + i + NST);
             }
             if (!ok) {
                 if (lane == 0) raise_fault(a.dev_error, PKV_FAULT_TIMEOUT);
@@ -403,7 +405,8 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 // the next item's first stages and query rows, before this item's epilogue
                 nx = decode(j1, f1);
 #pragma unroll 1
-                for (int j = 0; j < NST && j < nx.nb; ++j) issue(nx.g, ctr + j, __shfl_sync(FULL, entn0, j));
+                for (int j = 0; j < NST && j < nx.nb; ++j)
+                    issue(nx.g, ctr + j, __shfl_sync(FULL, entn0, j), nx.b0 + j);
                 load_rows(nx);  // every lane is past its last ldmatrix of the buffer
             }
             // epilogue: rows gid and gid+8 of each tile, straight from registers

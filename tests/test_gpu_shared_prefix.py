@@ -270,3 +270,33 @@ def test_plan_lists_every_item_once_largest_first(case):
     for s in range(S):
         assert nparts[s] == sum(1 for e in exp_pre if e[0] <= s < e[0] + e[1]) + \
             sum(1 for e in exp_suf if e[0] == s)
+
+
+# ----------------------------------------------- blocks of 64 to 256 tokens
+
+@pytest.mark.parametrize("BS", [64, 128, 256])
+def test_shared_prefix_large_blocks(BS):
+    """Blocks above 32 tokens are listed and staged as 32-row runs; the
+    prefix stays whole blocks and the combine checks the tables per block."""
+    ctx = _prefix_ctx(2 * BS, [0, 1, 31, 33, BS, BS + 7, 3 * BS])
+    groups = [(4, 2 * BS), (3, BS)]
+    w = _w(f"large{BS}", ctx, groups, 32, 8, 128, BS, seed=40 + BS // 64)
+    ref, _, _ = oracle_after_write(w)
+    for pt in (0, -1, BS):
+        dw = _run(w, pt)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, "bf16", f"BS {BS} partition {pt}")
+
+
+def test_shared_prefix_large_block_tables_that_differ_are_reported():
+    """Member 2 names its own third block where the group shares block 1:
+    the combine compares the tables per block (not per run) and reports it."""
+    BS = 64
+    ctx = _prefix_ctx(2 * BS, [10, 20, 30])
+    w = _w("large_bad", ctx, [(3, 2 * BS)], 16, 4, 128, BS, seed=47)
+    bt = w.block_tables.copy()
+    assert bt[2, 2] >= 0 and bt[2, 2] != bt[0, 1]
+    bt[2, 1] = bt[2, 2]
+    w.block_tables = bt
+    dw = _run(w, 0)
+    assert pagedkv.get_device_error(dw.pool) & pagedkv.FAULT_PREFIX
