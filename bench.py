@@ -346,6 +346,25 @@ def run_native(args, world: int, rank: int) -> dict | None:
     value = whole_job_rate(ab["kv_logical"] * args.steps, world, max_s) / 1e9
     seqs_per_s = whole_job_rate(w.num_seqs * args.steps, world, max_s)
 
+    # ---- the same step captured once in a CUDA graph and replayed (what a
+    # serving loop that replays its decode step pays; launch-bound batches gain)
+    graph_us = None
+    if world == 1:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = g0.elapsed_time(g1) * 1e3 / args.steps
+        del graph
+
     # ---- the plain decode kernel on the same batch (what prefix awareness buys)
     plain_cmp = None
     if shared and world == 1:
@@ -508,6 +527,9 @@ def run_native(args, world: int, rank: int) -> dict | None:
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
         # reported beside the KV bytes: the decode call's other traffic, the
         # cache write's time, and sequences per second of the decode call alone
+        "graph_replay": None if graph_us is None else {
+            "us_per_step": round(graph_us, 2),
+            "note": "the same step captured once in a CUDA graph, replayed back to back"},
         "side": {"q_bytes": ab["q"], "out_bytes": ab["out"], "block_table_bytes": ab["table"],
                  "context_len_bytes": w.num_seqs * 4, "new_kv_bytes": ab["new_kv"],
                  "reshape_and_cache_us": round(rc_us, 2),
