@@ -384,6 +384,18 @@ pkv_status pkv_bm_shared_prefix(const pkv_block_manager *bm, const int64_t *seq_
  */
 pkv_status pkv_get_device_error(const pkv_pool *pool, void *stream, uint32_t *fault_bits);
 
+/*
+ * Check of the kernels' watchdog: every shared-memory pipeline wait in the
+ * decode kernels gives up after a bound (2 s), records PKV_FAULT_TIMEOUT in
+ * the pool's error word and stops, so a copy that never lands cannot hang
+ * the GPU.  This call runs that same bounded wait on a barrier nothing
+ * arrives at, with limit_ns (1 us .. 2 s) as the bound: after it,
+ * pkv_get_device_error reports PKV_FAULT_TIMEOUT and the context is still
+ * usable.  The pool must have an error word.  Enqueued on `stream`; takes
+ * about limit_ns of GPU time.
+ */
+pkv_status pkv_check_bounded_wait(const pkv_pool *pool, long long limit_ns, void *stream);
+
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status status);
 

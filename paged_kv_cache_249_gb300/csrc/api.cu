@@ -399,6 +399,15 @@ pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *src, const int32
     return launch_copy_blocks(*pool, src, dst, num_pairs, static_cast<cudaStream_t>(stream));
 }
 
+pkv_status pkv_check_bounded_wait(const pkv_pool *pool, long long limit_ns, void *stream) {
+    if (!pool || pool->magic != kPoolMagic || !pool->dev_error) return PKV_ERR_INVALID_ARG;
+    if (limit_ns < 1000 || limit_ns > 2000000000ll) return PKV_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
+    if (dev != pool->device) return PKV_ERR_INVALID_ARG;
+    return launch_bounded_wait_check(pool->dev_error, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
 pkv_status pkv_get_device_error(const pkv_pool *pool, void *stream, uint32_t *fault_bits) {
     if (fault_bits) *fault_bits = 0;
     if (!pool || pool->magic != kPoolMagic) return PKV_ERR_INVALID_ARG;

@@ -99,6 +99,31 @@ pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const in
     return cuda_status(cudaGetLastError());
 }
 
+// ---------------------------------------------------- bounded-wait check
+//
+// Every pipeline wait in the decode kernels is bounded: past its limit the
+// kernel records PKV_FAULT_TIMEOUT in the caller's error word and stops, so
+// a copy that never lands cannot hang the GPU.  This kernel runs that same
+// bounded wait on an mbarrier nothing will ever arrive at, with the caller's
+// (short) limit, so a test or a deployment can watch the path work: the
+// wait gives up, the fault bit is set, and the context stays usable.
+__global__ void bounded_wait_check_kernel(int32_t *dev_error, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // phase 0 never completes: no thread arrives and no copy is in flight
+    const bool done = __all_sync(0xffffffffu, mbar_wait_for(&bar, 0, limit_ns));
+    if (!done && threadIdx.x == 0) raise_fault(dev_error, PKV_FAULT_TIMEOUT);
+}
+
+pkv_status launch_bounded_wait_check(int32_t *dev_error, long long limit_ns, cudaStream_t stream) {
+    bounded_wait_check_kernel<<<1, 32, 0, stream>>>(dev_error, (unsigned long long)limit_ns);
+    return cuda_status(cudaGetLastError());
+}
+
 // ------------------------------------------------------------ lse_combine
 //
 // A context split into partitions p = 0..P-1 has, per query head, normalised

@@ -93,14 +93,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned phase) {
 }
 
 // Wait for `phase` of `bar` to complete.  Returns false if the wait ran past
-// kWaitLimitNs (the caller then records PKV_FAULT_TIMEOUT and stops).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned phase) {
+// limit_ns (the caller then records PKV_FAULT_TIMEOUT and stops).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, unsigned phase,
+                                              unsigned long long limit_ns) {
     if (mbar_try_wait(bar, phase)) return true;
     const unsigned long long t0 = global_ns();
     for (unsigned it = 1;; ++it) {
         if (mbar_try_wait(bar, phase)) return true;
-        if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned phase) {
+    return mbar_wait_for(bar, phase, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------------- TMA

@@ -134,6 +134,7 @@ pkv_status launch_reshape_and_cache(const pkv_pool &pool, const void *key, const
                                     const int64_t *slot_mapping, int num_tokens,
                                     cudaStream_t stream);
 
+pkv_status launch_bounded_wait_check(int32_t *dev_error, long long limit_ns, cudaStream_t stream);
 pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const int32_t *dst,
                               int num_pairs, cudaStream_t stream);
 

@@ -37,7 +37,7 @@ EXPORTS = ["pkv_pool_bytes", "pkv_block_pool_init", "pkv_block_table_upload",
            "pkv_bm_block_tables", "pkv_bm_shared_prefix", "pkv_contiguous_cache_init",
            "pkv_contiguous_attention_decode", "pkv_shared_prefix_workspace_bytes",
            "pkv_paged_attention_decode_shared_prefix", "pkv_shared_prefix_plan",
-           "pkv_paged_attention_decode_shared_prefix_run"]
+           "pkv_paged_attention_decode_shared_prefix_run", "pkv_check_bounded_wait"]
 
 
 class PagedKVError(RuntimeError):
@@ -80,6 +80,7 @@ def load(path: Optional[str] = None):
         "pkv_decode_workspace_bytes": (Z, [I, I, I, I, I]),
         "pkv_paged_attention_decode": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, P, Z, I, P]),
         "pkv_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
+        "pkv_check_bounded_wait": (I, [PP, ctypes.c_longlong, P]),
         "pkv_paged_attention_decode_static": (I, [PP, P, I, P, I, I, I, P, I, P, I, F, I, I, P]),
         "pkv_copy_blocks": (I, [PP, P, P, I, P]),
         "pkv_contiguous_cache_init": (I, [PP, I, I, I, I, I, P, P, P, I, P]),
@@ -450,6 +451,14 @@ def get_device_error(pool: BlockPool, stream=None) -> int:
     if st not in (OK, ERR_DEVICE_FAULT):
         _check(st, "pkv_get_device_error")
     return int(bits.value)
+
+
+def check_bounded_wait(pool: BlockPool, limit_ns: int, stream=None) -> None:
+    """pkv_check_bounded_wait: run the kernels' bounded pipeline wait on a
+    barrier nothing arrives at, with limit_ns as the bound (it sets
+    FAULT_TIMEOUT in the pool's error word)."""
+    _check(load().pkv_check_bounded_wait(ctypes.byref(pool.desc), int(limit_ns), _stream(stream)),
+           "pkv_check_bounded_wait")
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,

@@ -253,3 +253,13 @@ def test_shared_prefix_plan_and_run_reject_bad_arguments_on_host(lib):
     assert run(pool, H=34) == U
     assert run(pool, ws=0x7010) == E                                  # not 256-byte aligned
     assert run(pool, S=0) == pagedkv.OK
+
+
+def test_bounded_wait_check_rejects_bad_arguments_on_host(lib):
+    E = pagedkv.ERR_INVALID_ARG
+    chk = lib.pkv_check_bounded_wait
+    assert chk(None, 1000000, None) == E
+    assert chk(ctypes.byref(_fake_pool()), 1000000, None) == E      # pool without an error word
+    fp = _fake_pool(dev_error=0x5000)
+    for limit in (0, 999, 2000000001, -5):
+        assert chk(ctypes.byref(fp), limit, None) == E, limit
