@@ -31,7 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 _lock = threading.Lock()
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 
 
 def compile_source(src: str, out: str) -> str:
@@ -91,7 +91,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return F32
     if t.dtype == torch.bfloat16:
         return BF16
-    raise TypeError(f"oracle supports float32 and bfloat16 storage, got {t.dtype}")
+    if t.dtype == torch.float16:
+        return F16
+    raise TypeError(f"oracle supports float32, bfloat16 and float16 storage, got {t.dtype}")
 
 
 def _cpu(t: torch.Tensor) -> torch.Tensor:

@@ -26,7 +26,7 @@
  *     z_j = scale * <q[s][h], K[j]>
  *     p_j = exp(z_j - max z) / sum_i exp(z_i - max z)
  *     out[s][h] = sum_j p_j V[j]
- * all in float64 on the exact input values (bf16 widened exactly).
+ * all in float64 on the exact input values (bf16 and fp16 widened exactly).
  * ctx = 0 yields a zero row (softmax over an empty set is undefined).
  *
  * Cache write: each new token t with slot = slot_mapping[t] >= 0 copies its
@@ -40,13 +40,32 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
 
-static int elem_size(int dtype) { return dtype == ORACLE_BF16 ? 2 : 4; }
+static int elem_size(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+
+/* Exact value of an IEEE binary16 bit pattern: sign, 5-bit exponent (bias
+ * 15), 10-bit fraction; exponent 0 holds the subnormals frac * 2^-24. */
+static double half_value(uint16_t h) {
+    const int sign = h >> 15, ex = (h >> 10) & 31, frac = h & 1023;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)frac, -24);
+    else if (ex == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), ex - 25);
+    return sign ? -v : v;
+}
 
 /* Exact widening of one stored element to float64.  bf16 is the top half of
  * an IEEE binary32, so shifting its 16 bits up gives the same value. */
 static double load_elem(const void *base, int dtype, size_t idx) {
+    if (dtype == ORACLE_F16) {
+        uint16_t h;
+        memcpy(&h, (const char *)base + idx * 2, 2);
+        return half_value(h);
+    }
     if (dtype == ORACLE_BF16) {
         uint16_t h;
         memcpy(&h, (const char *)base + idx * 2, 2);

@@ -48,7 +48,7 @@ META_SEED_BASE = 249100
 @dataclasses.dataclass
 class Workload:
     name: str
-    dtype: str                 # "f32" or "bf16": dtype of q, pools and new K/V
+    dtype: str                 # "f32", "bf16" or "f16": dtype of q, pools and new K/V
     num_seqs: int
     num_heads: int
     num_kv_heads: int
@@ -73,7 +73,7 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
 
     @property
     def elem_bytes(self) -> int:
@@ -133,7 +133,7 @@ def _normal_f32(ss: np.random.SeedSequence, n: int, threads: int = 0) -> np.ndar
 def _tensor(ss: np.random.SeedSequence, shape: Sequence[int], dtype: str) -> torch.Tensor:
     n = int(np.prod(shape)) if len(shape) else 1
     t = torch.from_numpy(_normal_f32(ss, n)).reshape(*shape)
-    return t if dtype == "f32" else t.to(torch.bfloat16)
+    return t if dtype == "f32" else t.to(torch.bfloat16 if dtype == "bf16" else torch.float16)
 
 
 def build(name: str, *, dtype: str, context_lens: Sequence[int], num_heads: int,

@@ -297,3 +297,38 @@ def test_reshape_negative_slot_is_skipped_bf16():
     assert torch.equal(kp[sm[0] // 4, :, sm[0] % 4], w.new_key[0])
     blk, off = divmod(int(w.slot_mapping[1]), 4)
     assert torch.equal(kp[blk, :, off], w.k_pool[blk, :, off])
+
+
+# ------------------------------------------------------------- fp16 input --
+
+def test_fp16_storage_is_widened_exactly():
+    """Every finite IEEE binary16 value, stored in a V pool, comes back from a
+    one-token context bit for bit as the value the format defines (checked
+    against numpy's own float16 conversion): sign, exponent bias, the
+    implicit bit and the subnormals all enter the oracle exactly."""
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    vals = bits.view(np.float16)
+    finite = vals[np.isfinite(vals)]
+    D = 128
+    rows = -(-finite.size // D)
+    v = np.zeros(rows * D, dtype=np.float16)
+    v[:finite.size] = finite
+    vp = torch.from_numpy(v.reshape(rows, 1, 1, D).copy())  # one-token blocks, one kv head
+    kp = torch.zeros_like(vp)
+    q = torch.zeros(rows, 1, D, dtype=torch.float16)
+    bt = np.arange(rows, dtype=np.int32).reshape(rows, 1)
+    out = oracle.paged_decode(q, kp, vp, bt, np.ones(rows, dtype=np.int32), 1.0, num_threads=4)
+    got = out.reshape(-1)[:finite.size]
+    assert np.array_equal(got, finite.astype(np.float64))
+
+
+def test_fp16_matches_brute_force():
+    """A small fp16 batch against the pure-Python brute force on the same
+    widened values."""
+    w = workload.build("pin_f16", dtype="f16", context_lens=[1, 5, 17, 40], num_heads=4,
+                       num_kv_heads=2, head_dim=64, block_size=16, data_seed=31, meta_seed=32)
+    out = oracle.paged_decode(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens, w.scale,
+                              num_threads=2)
+    ref = _brute.paged_decode(w.q.numpy(), w.k_pool.numpy(), w.v_pool.numpy(), w.block_tables,
+                              w.context_lens, w.scale)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
