@@ -53,7 +53,7 @@ typedef enum {
     PKV_ERR_OUT_OF_BLOCKS = 6  /* the block manager has no free block left */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
 
 /* Bits a kernel ORs into *pool->dev_error. */
 #define PKV_FAULT_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks): block skipped */
@@ -67,7 +67,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 /* Flags of pkv_paged_attention_decode. */
 #define PKV_DECODE_PATH_AUTO 0  /* tensor cores when the GQA group makes dense tiles */
 #define PKV_DECODE_PATH_FMA 1   /* CUDA-core dot products for every group size */
-#define PKV_DECODE_PATH_MMA 2   /* tensor-core tiles (bf16 only) for every group size */
+#define PKV_DECODE_PATH_MMA 2   /* tensor-core tiles (bf16 or fp16 pools) for every group size */
 
 /*
  * Block pool: K and V are separate device buffers, each laid out
@@ -104,7 +104,7 @@ size_t pkv_pool_bytes(int num_blocks, int block_size, int num_kv_heads, int head
  * non-zero clears both pools and the error word on `stream`.
  * Supported: block_size in {16, 32, 64, 128, 256} (the page's range of
  * roughly 16 to 256 tokens; blocks above 32 tokens are staged in runs of 32
- * rows); head_dim in {64, 128}; dtype F32 or BF16;
+ * rows); head_dim in {64, 128}; dtype F32, BF16 or F16;
  * num_blocks*num_kv_heads*block_size < 2^31.
  */
 pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, int num_kv_heads,
@@ -156,7 +156,10 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
  * A sequence with context length 0 gets a zero row.
  *
  * query: device [num_seqs][num_heads][head_dim] in the pool dtype.
- * out: device [num_seqs][num_heads][head_dim] in out_dtype (F32 or BF16).
+ * out: device [num_seqs][num_heads][head_dim] in out_dtype (F32, BF16 or
+ *   F16).  Scores and sums are fp32 whatever the storage type; tensor-core
+ *   tiles (PKV_DECODE_PATH_MMA, and AUTO for groups of 4 or more) take BF16
+ *   or F16 pools.
  * block_tables: device int32 [num_seqs][max_blocks_per_seq].
  * context_lens: device int32 [num_seqs].
  * max_context_len: host upper bound on every context length (grid sizing;
@@ -270,8 +273,8 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * each sequence's own blocks), -1 = one part each, > 0 = parts of that many tokens (a
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
- * holds the work list, so every call needs one.  Supported: bf16 pools,
- * num_heads / num_kv_heads in 1..16, out_dtype F32 or BF16.
+ * holds the work list, so every call needs one.  Supported: BF16 or F16
+ * pools, num_heads / num_kv_heads in 1..16, out_dtype F32, BF16 or F16.
  */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_context_len, int max_prefix_len,

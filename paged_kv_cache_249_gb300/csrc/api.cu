@@ -44,13 +44,14 @@ bool encode_pool_map(CUtensorMap *map, void *base, int rows, int head_dim, int b
                      pkv_dtype dtype) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const int elem = dtype == PKV_BF16 ? 2 : 4;
+    const int elem = dtype == PKV_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)head_dim * elem};
     const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)stage_rows(block_size)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+    CUresult r = fn(map, dtype == PKV_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                         : dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                     2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -124,15 +125,15 @@ const char *pkv_status_string(pkv_status s) {
 size_t pkv_pool_bytes(int num_blocks, int block_size, int num_kv_heads, int head_dim,
                       pkv_dtype dtype) {
     if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
-    if (dtype != PKV_F32 && dtype != PKV_BF16) return 0;
-    return (size_t)num_blocks * num_kv_heads * block_size * head_dim * (dtype == PKV_BF16 ? 2 : 4);
+    if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_F16) return 0;
+    return (size_t)num_blocks * num_kv_heads * block_size * head_dim * (dtype == PKV_F32 ? 4 : 2);
 }
 
 pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, int num_kv_heads,
                                int head_dim, pkv_dtype dtype, void *k_pool, void *v_pool,
                                int32_t *dev_error, int zero_fill, void *stream) {
     if (!pool || !k_pool || !v_pool) return PKV_ERR_INVALID_ARG;
-    if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_F16) return PKV_ERR_INVALID_ARG;
     if (num_blocks <= 0 || num_kv_heads <= 0 || block_size <= 0 || head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     if (!valid_geometry(num_blocks, block_size, num_kv_heads, head_dim)) return PKV_ERR_UNSUPPORTED;
@@ -241,7 +242,8 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
         return PKV_ERR_INVALID_ARG;
     if (num_kv_heads != pool->num_kv_heads || num_heads % num_kv_heads != 0)
         return PKV_ERR_INVALID_ARG;
-    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16 && out_dtype != PKV_F16)
+        return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if (flags != PKV_DECODE_PATH_AUTO && flags != PKV_DECODE_PATH_FMA &&
         flags != PKV_DECODE_PATH_MMA)
@@ -257,11 +259,11 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     const int group = num_heads / num_kv_heads;
     if (group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
     if (num_kv_heads > 65535 || num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid y
-    const bool bf16 = pool->dtype == PKV_BF16;
-    bool mma = bf16 && group >= 4;
+    const bool half16 = pool->dtype != PKV_F32;  // bf16 or fp16: tensor-core tiles possible
+    bool mma = half16 && group >= 4;
     if (flags == PKV_DECODE_PATH_FMA) mma = false;
     if (flags == PKV_DECODE_PATH_MMA) {
-        if (!bf16) return PKV_ERR_UNSUPPORTED;
+        if (!half16) return PKV_ERR_UNSUPPORTED;
         mma = true;
     }
     int dev = 0;
@@ -291,7 +293,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = pool->num_blocks;
     a.ctx_cap = ctx_cap;
-    a.out_bf16 = out_dtype == PKV_BF16;
+    a.out_dtype = out_dtype;
     a.contig = contig ? 1 : 0;
     a.unit_shift = unit_shift;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -336,8 +338,10 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     L.device = dev;
 
     pkv_status st;
-    if (bf16)
+    if (pool->dtype == PKV_BF16)
         st = pool->head_dim == 64 ? launch_decode_bf16_d64(L) : launch_decode_bf16_d128(L);
+    else if (pool->dtype == PKV_F16)
+        st = pool->head_dim == 64 ? launch_decode_f16_d64(L) : launch_decode_f16_d128(L);
     else
         st = pool->head_dim == 64 ? launch_decode_f32_d64(L) : launch_decode_f32_d128(L);
     if (st != PKV_OK || parts <= 1) return st;

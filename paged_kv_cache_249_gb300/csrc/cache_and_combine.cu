@@ -47,7 +47,7 @@ pkv_status launch_reshape_and_cache(const pkv_pool &pool, const void *key, const
                                     const int64_t *slot_mapping, int num_tokens,
                                     cudaStream_t stream) {
     if (num_tokens == 0) return PKV_OK;
-    const int elem = pool.dtype == PKV_BF16 ? 2 : 4;
+    const int elem = pool.dtype == PKV_F32 ? 4 : 2;
     const int chunks = pool.head_dim * elem / 16;
     const long long total = (long long)num_tokens * pool.num_kv_heads * chunks;
     long long blocks = (total + 255) / 256;
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256)
 
 pkv_status launch_copy_blocks(const pkv_pool &pool, const int32_t *src, const int32_t *dst,
                               int num_pairs, cudaStream_t stream) {
-    const int elem = pool.dtype == PKV_BF16 ? 2 : 4;
+    const int elem = pool.dtype == PKV_F32 ? 4 : 2;
     const long long chunks =
         (long long)pool.num_kv_heads * pool.block_size * pool.head_dim * elem / 16;
     long long blocks = (chunks * num_pairs + 255) / 256;
@@ -172,10 +172,7 @@ __device__ __forceinline__ float comb_max(const CombRow &r, float *red) {
 }
 
 __device__ __forceinline__ void comb_store(const DecodeArgs &a, size_t oi, float res) {
-    if (a.out_bf16)
-        reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(res);
-    else
-        reinterpret_cast<float *>(a.out)[oi] = res;
+    store_out(a.out, oi, res, a.out_dtype);
 }
 
 // Few partitions: one warp per (sequence, head), each lane owning D/32

@@ -18,9 +18,9 @@
 // by 2^(m_old - m_new) whenever the max grows.  Two compute paths:
 //   * FMA: CUDA-core dot products; a row of D elements is spread over
 //     LPT lanes (16-byte chunks), reduced with xor shuffles.
-//   * MMA: bf16 mma.sync m16n8k16 with the G query rows padded to 16:
+//   * MMA: bf16 or fp16 mma.sync m16n8k16 with the G query rows padded to 16:
 //     S = Q K^T per block from ldmatrix'd K, then O += P V with P split into
-//     a bf16 high part and a bf16 remainder so the weights keep ~16 bits.
+//     a 16-bit high part and a 16-bit remainder so the weights keep ~16 bits.
 // At the end the per-warp states are merged with a log-sum-exp combine in
 // shared memory; a partitioned (split) context writes normalised partials
 // and their log2-sum-exp, which lse_combine reduces.
@@ -41,6 +41,10 @@ struct ElemTraits<float> {
 };
 template <>
 struct ElemTraits<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+};
+template <>
+struct ElemTraits<__half> {
     static constexpr int kBytes = 2;
 };
 
@@ -101,6 +105,7 @@ __device__ __forceinline__ float load_as_float(const float *p) { return *p; }
 __device__ __forceinline__ float load_as_float(const __nv_bfloat16 *p) {
     return __bfloat162float(*p);
 }
+__device__ __forceinline__ float load_as_float(const __half *p) { return __half2float(*p); }
 
 // Load 16 bytes of q / K / V and widen to EPC floats.
 template <typename T>
@@ -122,6 +127,17 @@ __device__ __forceinline__ void widen16<__nv_bfloat16>(const uint4 &v, float *f)
     f[5] = bf16_hi(v.z);
     f[6] = bf16_lo(v.w);
     f[7] = bf16_hi(v.w);
+}
+template <>
+__device__ __forceinline__ void widen16<__half>(const uint4 &v, float *f) {
+    f[0] = f16_lo(v.x);
+    f[1] = f16_hi(v.x);
+    f[2] = f16_lo(v.y);
+    f[3] = f16_hi(v.y);
+    f[4] = f16_lo(v.z);
+    f[5] = f16_hi(v.z);
+    f[6] = f16_lo(v.w);
+    f[7] = f16_hi(v.w);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -280,9 +296,9 @@ struct FmaPath {
 
 // ------------------------------------------------------------ MMA compute
 
-template <int D, int BS, int RG>
+template <typename T, int D, int BS, int RG>
 struct MmaPath {
-    using T = __nv_bfloat16;
+    using MM = Mma16<T>;
     static constexpr int GP = RG;       // rows exported: 8 when the group fits rows g < 8
     static constexpr int KS = D / 16;   // k-steps of the QK^T product
     static constexpr int NT = BS / 8;   // token n-tiles per block
@@ -324,8 +340,8 @@ struct MmaPath {
             for (int kc = 0; kc < D / 32; ++kc) {
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kaddr + swz_offset<BS>(row, kc * 4 + (lane >> 3)), b0, b1, b2, b3);
-                mma_bf16_16816(s[nt], qa[2 * kc], b0, b1);
-                mma_bf16_16816(s[nt], qa[2 * kc + 1], b2, b3);
+                MM::mma(s[nt], qa[2 * kc], b0, b1);
+                MM::mma(s[nt], qa[2 * kc + 1], b2, b3);
             }
         }
         float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
@@ -372,16 +388,16 @@ struct MmaPath {
         }
 #pragma unroll
         for (int kt = 0; kt < BS / 16; ++kt) {
-            // P as A fragments: high bf16 part and the bf16 of the remainder
+            // P as A fragments: its 16-bit high part and the 16-bit remainder
             uint32_t ph[4], pl[4];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const float *sv = s[2 * kt + j];
-                ph[2 * j] = pack_bf16(sv[0], sv[1]);
-                ph[2 * j + 1] = pack_bf16(sv[2], sv[3]);
-                pl[2 * j] = pack_bf16(sv[0] - bf16_lo(ph[2 * j]), sv[1] - bf16_hi(ph[2 * j]));
+                ph[2 * j] = MM::pack(sv[0], sv[1]);
+                ph[2 * j + 1] = MM::pack(sv[2], sv[3]);
+                pl[2 * j] = MM::pack(sv[0] - MM::lo(ph[2 * j]), sv[1] - MM::hi(ph[2 * j]));
                 pl[2 * j + 1] =
-                    pack_bf16(sv[2] - bf16_lo(ph[2 * j + 1]), sv[3] - bf16_hi(ph[2 * j + 1]));
+                    MM::pack(sv[2] - MM::lo(ph[2 * j + 1]), sv[3] - MM::hi(ph[2 * j + 1]));
             }
             const bool partial = nvalid < (kt + 1) * 16;
             const int t0 = kt * 16 + 2 * tig;
@@ -401,10 +417,10 @@ struct MmaPath {
                 b2 &= mlo;
                 b1 &= mhi;
                 b3 &= mhi;
-                mma_bf16_16816(o[2 * np], ph, b0, b1);
-                mma_bf16_16816(o[2 * np], pl, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], ph, b2, b3);
-                mma_bf16_16816(o[2 * np + 1], pl, b2, b3);
+                MM::mma(o[2 * np], ph, b0, b1);
+                MM::mma(o[2 * np], pl, b0, b1);
+                MM::mma(o[2 * np + 1], ph, b2, b3);
+                MM::mma(o[2 * np + 1], pl, b2, b3);
             }
         }
     }
@@ -443,7 +459,11 @@ struct PathOf {
 };
 template <int D, int BS, int GP>
 struct PathOf<__nv_bfloat16, D, BS, GP, true> {
-    using type = MmaPath<D, BS, GP>;
+    using type = MmaPath<__nv_bfloat16, D, BS, GP>;
+};
+template <int D, int BS, int GP>
+struct PathOf<__half, D, BS, GP, true> {
+    using type = MmaPath<__half, D, BS, GP>;
 };
 
 template <typename T, int D, int BS, int GP, bool MMA>
@@ -602,10 +622,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         const float res = L > 0.f ? O / L : 0.f;
         if (!split) {
             const size_t oi = (head0 + r) * D + d;
-            if (a.out_bf16)
-                reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(res);
-            else
-                reinterpret_cast<float *>(a.out)[oi] = res;
+            store_out(a.out, oi, res, a.out_dtype);
         } else {
             const size_t pi = (head0 + r) * a.num_parts + part;
             a.ws_o[pi * D + d] = res;

@@ -1,10 +1,11 @@
 // pkv_device.cuh -- device-side building blocks for sm_103a: mbarrier waits
-// with a time bound, TMA tiled loads, ldmatrix / mma.sync wrappers, bf16
-// packing and the device error word.
+// with a time bound, TMA tiled loads, ldmatrix / mma.sync wrappers, bf16 and
+// fp16 packing and the device error word.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -160,6 +161,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A(16x16 fp16, row) * B(16x8 fp16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // ------------------------------------------------------------------ numbers
 
 // 2^x with the hardware approximation (ex2.approx, about 2 ulp); 2^-inf = 0.
@@ -177,6 +188,62 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Two fp16 in one 32-bit word -> the floats they denote, and back.
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// The 16-bit element types the tensor-core paths take: the mma.sync of that
+// type (A and B of one type) and the packing of P into its A fragments.
+template <typename T>
+struct Mma16;
+template <>
+struct Mma16<__nv_bfloat16> {
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        mma_bf16_16816(d, a, b0, b1);
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16(lo, hi); }
+    static __device__ __forceinline__ float lo(uint32_t w) { return bf16_lo(w); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return bf16_hi(w); }
+};
+template <>
+struct Mma16<__half> {
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        mma_f16_16816(d, a, b0, b1);
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16(lo, hi); }
+    static __device__ __forceinline__ float lo(uint32_t w) { return f16_lo(w); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return f16_hi(w); }
+};
+
+// Store one output value in the caller's output type (a pkv_dtype).
+__device__ __forceinline__ void store_out(void *out, size_t i, float v, int out_dtype) {
+    if (out_dtype == PKV_BF16)
+        reinterpret_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+    else if (out_dtype == PKV_F16)
+        reinterpret_cast<__half *>(out)[i] = __float2half_rn(v);
+    else
+        reinterpret_cast<float *>(out)[i] = v;
+}
+// Two adjacent output values (i even).
+__device__ __forceinline__ void store_out2(void *out, size_t i, float v0, float v1, int out_dtype) {
+    if (out_dtype == PKV_BF16)
+        *reinterpret_cast<uint32_t *>(reinterpret_cast<__nv_bfloat16 *>(out) + i) = pack_bf16(v0, v1);
+    else if (out_dtype == PKV_F16)
+        *reinterpret_cast<uint32_t *>(reinterpret_cast<__half *>(out) + i) = pack_f16(v0, v1);
+    else
+        *reinterpret_cast<float2 *>(reinterpret_cast<float *>(out) + i) = make_float2(v0, v1);
 }
 
 }  // namespace pkv

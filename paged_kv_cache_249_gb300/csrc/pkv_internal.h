@@ -34,7 +34,7 @@ struct DecodeArgs {
     int ctx_cap;                // min(max_blocks_per_seq * BS, max_context_len)
     int part_blocks;            // KV blocks per partition (one CTA each)
     int num_parts;              // gridDim.z: partitions of the longest allowed context
-    int out_bf16;
+    int out_dtype;              // pkv_dtype of out
     int contig;                 // 1: contiguous cache, block b of (s, g) is row run (s*Hkv+g)*num_blocks+b
     int unit_shift;             // a pool block is 2^unit_shift staged runs of BS rows (blocks over 32 rows)
     float scale_log2;           // scale * log2(e)
@@ -92,7 +92,7 @@ struct SpArgs {
     int max_blocks_per_seq;
     int num_blocks;
     int num_slots;
-    int out_bf16;
+    int out_dtype;              // pkv_dtype of out
     float scale_log2;
 };
 
@@ -119,13 +119,17 @@ struct SpLaunch {
     int device;
 };
 
-pkv_status launch_shared_prefix_d64(const SpLaunch &L);
-pkv_status launch_shared_prefix_d128(const SpLaunch &L);
+pkv_status launch_shared_prefix_d64(const SpLaunch &L);       // bf16 pools
+pkv_status launch_shared_prefix_d128(const SpLaunch &L);      // bf16 pools
+pkv_status launch_shared_prefix_f16_d64(const SpLaunch &L);
+pkv_status launch_shared_prefix_f16_d128(const SpLaunch &L);
 
 pkv_status launch_decode_f32_d64(const DecodeLaunch &L);
 pkv_status launch_decode_f32_d128(const DecodeLaunch &L);
 pkv_status launch_decode_bf16_d64(const DecodeLaunch &L);
 pkv_status launch_decode_bf16_d128(const DecodeLaunch &L);
+pkv_status launch_decode_f16_d64(const DecodeLaunch &L);
+pkv_status launch_decode_f16_d128(const DecodeLaunch &L);
 
 pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, int block_size,
                               cudaStream_t stream);

@@ -355,10 +355,7 @@ __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs
     const size_t oi = (size_t)wid * D + lane * PER;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-        if (a.out_bf16)
-            reinterpret_cast<__nv_bfloat16 *>(a.out)[oi + j] = __float2bfloat16_rn(res[j]);
-        else
-            reinterpret_cast<float *>(a.out)[oi + j] = res[j];
+        store_out(a.out, oi + j, res[j], a.out_dtype);
     }
 }
 
@@ -401,7 +398,7 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
         (partition_tokens > 0 && partition_tokens % c.BS != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (pool->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;  // tensor-core tiles: bf16 or fp16
     // blocks above kMaxStageRows tokens are staged (and listed) in runs
     c.U = c.BS < kMaxStageRows ? c.BS : kMaxStageRows;
     c.unit_shift = 0;
@@ -493,7 +490,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = pool->num_blocks;
     a.num_slots = c.z.slots;
-    a.out_bf16 = out_dtype == PKV_BF16;
+    a.out_dtype = out_dtype;
     a.scale_log2 = scale * 1.4426950408889634f;
 
     CUtensorMap maps[2];
@@ -507,7 +504,9 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     L.stream = st;
     L.device = c.dev;
     const pkv_status s1 =
-        pool->head_dim == 64 ? launch_shared_prefix_d64(L) : launch_shared_prefix_d128(L);
+        pool->dtype == PKV_F16
+            ? (pool->head_dim == 64 ? launch_shared_prefix_f16_d64(L) : launch_shared_prefix_f16_d128(L))
+            : (pool->head_dim == 64 ? launch_shared_prefix_d64(L) : launch_shared_prefix_d128(L));
     if (s1 != PKV_OK) return s1;
 
     // the combine waits for the decode grid in griddepcontrol.wait, then
@@ -522,7 +521,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
 
 bool sp_out_args_ok(void *out, pkv_dtype out_dtype, const void *query, const int32_t *block_tables,
                     float scale) {
-    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return false;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16 && out_dtype != PKV_F16) return false;
     if (!std::isfinite(scale)) return false;
     if (!out || !query || !block_tables) return false;
     return aligned(out, 16) && aligned(query, 16) && aligned(block_tables, 4);

@@ -5,6 +5,6 @@
 
 namespace pkv {
 
-pkv_status launch_shared_prefix_d128(const SpLaunch &L) { return launch_sp_d<128>(L); }
+pkv_status launch_shared_prefix_d128(const SpLaunch &L) { return launch_sp_d<__nv_bfloat16, 128>(L); }
 
 }  // namespace pkv

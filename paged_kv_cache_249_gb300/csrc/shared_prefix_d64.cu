@@ -5,6 +5,6 @@
 
 namespace pkv {
 
-pkv_status launch_shared_prefix_d64(const SpLaunch &L) { return launch_sp_d<64>(L); }
+pkv_status launch_shared_prefix_d64(const SpLaunch &L) { return launch_sp_d<__nv_bfloat16, 64>(L); }
 
 }  // namespace pkv

@@ -36,8 +36,8 @@ constexpr int kSpSmemTarget = 112 * 1024;
 
 template <int D, int BS>
 struct SpSmem {
-    using Gm = Geom<__nv_bfloat16, D, BS>;
-    static constexpr int kQ = kSpRowsMax * D * 2;  // a warp's query rows (bf16, swizzled slabs)
+    using Gm = Geom<__nv_bfloat16, D, BS>;  // sizes only: the same for fp16
+    static constexpr int kQ = kSpRowsMax * D * 2;  // a warp's query rows (16-bit, swizzled slabs)
     static constexpr int kMisc = 256;
     static constexpr int kFixed = kSpWarps * kQ + kMisc + 1024;
     static constexpr int kStagesFit = (kSpSmemTarget - kFixed) / (kSpWarps * Gm::kStageBytes);
@@ -71,10 +71,11 @@ struct SpItem {
 // Online-softmax attention of up to two 16-row tiles of query rows against
 // 16-token sub-blocks of K and V staged in shared memory.  The query tile is
 // read from shared memory with ldmatrix (it would not fit in registers next
-// to two tiles of accumulators); P is split into a bf16 high part and a bf16
+// to two tiles of accumulators); P is split into a 16-bit high part and a 16-bit
 // remainder so the weights keep about 16 bits.
-template <int D, int BS>
+template <typename T, int D, int BS>
 struct SpMma {
+    using MM = Mma16<T>;
     static constexpr int ND = D / 8;  // n-tiles of O
     float o[2][ND][4];
     float m[2][2], l[2][2];  // [tile][row gid / gid+8]; l is lane-partial
@@ -121,8 +122,8 @@ struct SpMma {
                         b1, b2, b3);
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
-                    mma_bf16_16816(s[t][nt], qa[t][0], b0, b1);
-                    mma_bf16_16816(s[t][nt], qa[t][1], b2, b3);
+                    MM::mma(s[t][nt], qa[t][0], b0, b1);
+                    MM::mma(s[t][nt], qa[t][1], b2, b3);
                 }
             }
         }
@@ -173,11 +174,11 @@ struct SpMma {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const float *sv = s[t][j];
-                ph[t][2 * j] = pack_bf16(sv[0], sv[1]);
-                ph[t][2 * j + 1] = pack_bf16(sv[2], sv[3]);
-                pl[t][2 * j] = pack_bf16(sv[0] - bf16_lo(ph[t][2 * j]), sv[1] - bf16_hi(ph[t][2 * j]));
+                ph[t][2 * j] = MM::pack(sv[0], sv[1]);
+                ph[t][2 * j + 1] = MM::pack(sv[2], sv[3]);
+                pl[t][2 * j] = MM::pack(sv[0] - MM::lo(ph[t][2 * j]), sv[1] - MM::hi(ph[t][2 * j]));
                 pl[t][2 * j + 1] =
-                    pack_bf16(sv[2] - bf16_lo(ph[t][2 * j + 1]), sv[3] - bf16_hi(ph[t][2 * j + 1]));
+                    MM::pack(sv[2] - MM::lo(ph[t][2 * j + 1]), sv[3] - MM::hi(ph[t][2 * j + 1]));
             }
         }
         // O += P V; rows past the context may hold stale bits (even NaN): zero them
@@ -200,10 +201,10 @@ struct SpMma {
             b3 &= mhi;
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
-                mma_bf16_16816(o[t][2 * np], ph[t], b0, b1);
-                mma_bf16_16816(o[t][2 * np], pl[t], b0, b1);
-                mma_bf16_16816(o[t][2 * np + 1], ph[t], b2, b3);
-                mma_bf16_16816(o[t][2 * np + 1], pl[t], b2, b3);
+                MM::mma(o[t][2 * np], ph[t], b0, b1);
+                MM::mma(o[t][2 * np], pl[t], b0, b1);
+                MM::mma(o[t][2 * np + 1], ph[t], b2, b3);
+                MM::mma(o[t][2 * np + 1], pl[t], b2, b3);
             }
         }
     }
@@ -222,11 +223,11 @@ struct SpMma {
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, int BS>
+template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kSpWarps * 32)
     shared_prefix_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                 const __grid_constant__ CUtensorMap tmv, const SpArgs a) {
-    using Gm = Geom<__nv_bfloat16, D, BS>;
+    using Gm = Geom<T, D, BS>;
     using Sm = SpSmem<D, BS>;
     constexpr int NST = Sm::NST;
     constexpr int QCH = D * 2 / 16;  // 16-byte chunks per query row
@@ -313,13 +314,13 @@ __global__ void __launch_bounds__(kSpWarps * 32)
         }
     };
     // the item's query rows into the warp's buffer (zero rows pad the last tile)
-    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+    const T *qg = reinterpret_cast<const T *>(a.q);
     auto load_rows = [&](const SpItem &t) {
         const int rows_pad = t.R > 16 ? 32 : 16;
 #pragma unroll 2
         for (int idx = lane; idx < rows_pad * QCH; idx += 32) {
             const int r = idx / QCH, c = idx - r * QCH;
-            const __nv_bfloat16 *src = qg;
+            const T *src = qg;
             int bytes = 0;
             if (r < t.R) {
                 const int sq = t.seq0 + r / G, h = t.g * G + r % G;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
         cp_async_commit();
     };
 
-    SpMma<D, BS> path;
+    SpMma<T, D, BS> path;
     unsigned ctr = 0;  // blocks this warp has consumed (stage ring position, across items)
     int j0 = fetch();
     if (j0 < total) {
@@ -430,13 +431,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                             const float2 v = make_float2(path.o[t][n][2 * hr] * invL,
                                                          path.o[t][n][2 * hr + 1] * invL);
                             if (npr == 1) {
-                                if (a.out_bf16)
-                                    *reinterpret_cast<uint32_t *>(
-                                        reinterpret_cast<__nv_bfloat16 *>(a.out) + sh * D + d) =
-                                        pack_bf16(v.x, v.y);
-                                else
-                                    *reinterpret_cast<float2 *>(reinterpret_cast<float *>(a.out) +
-                                                                sh * D + d) = v;
+                                store_out2(a.out, sh * D + d, v.x, v.y, a.out_dtype);
                             } else {
                                 const size_t pi = sh * a.num_slots + it.slot;
                                 *reinterpret_cast<float2 *>(a.ws_o + pi * D + d) = v;
@@ -459,9 +454,9 @@ __global__ void __launch_bounds__(kSpWarps * 32)
     griddep_launch();
 }
 
-template <int D, int BS>
+template <typename T, int D, int BS>
 pkv_status launch_sp_one(const SpLaunch &L) {
-    auto kern = shared_prefix_decode_kernel<D, BS>;
+    auto kern = shared_prefix_decode_kernel<T, D, BS>;
     constexpr int smem = SpSmem<D, BS>::kBytes;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     static unsigned long long done_mask = 0ull;
@@ -485,11 +480,11 @@ pkv_status launch_sp_one(const SpLaunch &L) {
         launch_dependent(kern, dim3(grid), dim3(kSpWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }
 
-template <int D>
+template <typename T, int D>
 pkv_status launch_sp_d(const SpLaunch &L) {
     switch (L.block_size) {
-        case 16: return launch_sp_one<D, 16>(L);
-        case 32: return launch_sp_one<D, 32>(L);
+        case 16: return launch_sp_one<T, D, 16>(L);
+        case 32: return launch_sp_one<T, D, 32>(L);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_FAULT,
  ERR_OUT_OF_BLOCKS) = range(7)
 # pkv_dtype
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 # device fault bits
 FAULT_BLOCK_ID, FAULT_SLOT, FAULT_CONTEXT, FAULT_TIMEOUT, FAULT_PREFIX = 1, 2, 4, 8, 16
 # decode paths
@@ -136,6 +136,8 @@ def _dtype_code(dt: torch.dtype) -> int:
         return F32
     if dt == torch.bfloat16:
         return BF16
+    if dt == torch.float16:
+        return F16
     raise TypeError(f"unsupported dtype {dt}")
 
 

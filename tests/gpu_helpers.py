@@ -7,7 +7,9 @@ import torch
 import oracle
 from paged_kv_cache_249_gb300 import pagedkv
 
-TOL = {"f32": 1e-5, "bf16": 2e-3}
+# max-abs tolerances by input storage: fp32 1e-5 and bf16 2e-3 (fp32
+# accumulation); fp16 inputs take the 16-bit input tolerance as well
+TOL = {"f32": 1e-5, "bf16": 2e-3, "f16": 2e-3}
 
 
 def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
@@ -15,6 +17,14 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
     e = np.floor(np.log2(ax))
     return np.ldexp(1.0, (e - 8).astype(np.int64))  # ulp = 2^(e-7); half = 2^(e-8)
+
+
+def f16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half an fp16 ulp at |x| (what storing an fp32 result as fp16 may add;
+    the subnormal spacing 2^-24 below 2^-14)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -14)
+    e = np.floor(np.log2(ax))
+    return np.ldexp(1.0, (e - 11).astype(np.int64))  # ulp = 2^(e-10); half = 2^(e-11)
 
 
 def oracle_after_write(w, seqs=None):
@@ -40,8 +50,8 @@ def assert_close(out: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "")
     tol = TOL[dtype]
     got = out.double().cpu().numpy()
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
-    if out.dtype == torch.bfloat16:
-        bound = tol + bf16_half_ulp(ref)
+    if out.dtype in (torch.bfloat16, torch.float16):
+        bound = tol + (bf16_half_ulp(ref) if out.dtype == torch.bfloat16 else f16_half_ulp(ref))
         bad = np.abs(got - ref) > bound
         assert not bad.any(), f"{what}: {bad.sum()} elements beyond tol+half-ulp, max err " \
                               f"{np.abs(got - ref).max():.3g}"

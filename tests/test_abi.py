@@ -66,6 +66,8 @@ def test_sizes_and_strings(lib):
     assert lib.pkv_pool_bytes(10, 16, 8, 128, pagedkv.BF16) == 10 * 16 * 8 * 128 * 2
     assert lib.pkv_pool_bytes(10, 16, 8, 64, pagedkv.F32) == 10 * 16 * 8 * 64 * 4
     assert lib.pkv_pool_bytes(0, 16, 8, 64, pagedkv.F32) == 0
+    assert lib.pkv_pool_bytes(10, 16, 8, 128, pagedkv.F16) == 10 * 16 * 8 * 128 * 2
+    assert lib.pkv_pool_bytes(10, 16, 8, 128, 3) == 0  # no such dtype
     for s in range(6):
         assert lib.pkv_status_string(s)
     # split-K partials: S*H*P*(D+1) floats, each part rounded to 256 bytes

@@ -28,7 +28,7 @@ def _w(dtype, D, BS, H, Hkv, ctx=RAGGED, seed=0, **kw):
 # ------------------------------------------------------------ cache write --
 
 @pytest.mark.parametrize("dtype,D,BS", [("f32", 64, 16), ("bf16", 128, 16), ("bf16", 64, 32),
-                                        ("f32", 128, 32)])
+                                        ("f32", 128, 32), ("f16", 128, 16), ("f16", 64, 64)])
 def test_reshape_and_cache_bit_exact(dtype, D, BS):
     w = _w(dtype, D, BS, 8, 4, ctx=[1, 16, 17, 40, 64, 65], pool_blocks=30)
     sm = w.slot_mapping.copy()
@@ -209,3 +209,41 @@ def test_large_blocks_equal_small_blocks_bitwise():
         assert pagedkv.get_device_error(dw.pool) == 0
         outs.append(dw.out.cpu())
     assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+
+
+# ------------------------------------------------------------- fp16 pools
+
+F16_CASES = [
+    # D, BS, H, Hkv
+    (128, 16, 32, 32),
+    (128, 16, 32, 8),
+    (64, 32, 16, 2),
+    (128, 64, 16, 4),
+    (64, 16, 6, 2),
+]
+
+
+@pytest.mark.parametrize("case", F16_CASES, ids=lambda c: "_".join(map(str, c)))
+def test_f16_decode_matches_oracle(case):
+    """fp16 pools and queries: CUDA-core and fp16 tensor-core paths, whole
+    and split contexts, against the oracle on the same fp16 values."""
+    D, BS, H, Hkv = case
+    w = _w("f16", D, BS, H, Hkv, seed=500 + F16_CASES.index(case))
+    ref, _, _ = oracle_after_write(w)
+    for pt in (-1, 0, 2 * BS):
+        for path in (pagedkv.PATH_AUTO, pagedkv.PATH_FMA, pagedkv.PATH_MMA):
+            dw = run_decode(w, path=path, partition_tokens=pt)
+            assert pagedkv.get_device_error(dw.pool) == 0
+            assert_close(dw.out, ref, "f16", f"{case} path={path} partition={pt}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_f16_output(dtype):
+    """An fp16 output is the fp32 result rounded once to fp16."""
+    w = _w(dtype, 128, 16, 16, 4, seed=520)
+    ref, _, _ = oracle_after_write(w)
+    dw16 = run_decode(w, partition_tokens=128, out_dtype=torch.float16)
+    assert_close(dw16.out, ref, dtype, "fp16 output")
+    dw32 = run_decode(w, partition_tokens=128, out_dtype=torch.float32)
+    assert torch.equal(dw32.out.to(torch.float16).cpu().view(torch.int16),
+                       dw16.out.cpu().view(torch.int16))

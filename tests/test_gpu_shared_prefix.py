@@ -300,3 +300,17 @@ def test_shared_prefix_large_block_tables_that_differ_are_reported():
     w.block_tables = bt
     dw = _run(w, 0)
     assert pagedkv.get_device_error(dw.pool) & pagedkv.FAULT_PREFIX
+
+
+# ------------------------------------------------------------- fp16 pools
+
+@pytest.mark.parametrize("case", ["g4_ragged_groups", "g8_two_items", "d64_bs32"])
+def test_shared_prefix_f16(case):
+    ctx, groups, H, Hkv, D, BS = CASES[case]
+    w = workload.build(case, dtype="f16", context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
+                       head_dim=D, block_size=BS, data_seed=5300, meta_seed=6300, groups=groups)
+    ref, _, _ = oracle_after_write(w)
+    for out_dtype in (torch.float32, torch.float16):
+        dw = _run(w, 0, out_dtype)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, "f16", f"{case} fp16 pools, out {out_dtype}")
