@@ -33,9 +33,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Rows of one staged run of a block: the whole block up to kMaxStageRows;
-// a larger block (64, 128 or 256 rows) is staged in runs of kMaxStageRows.
-int stage_rows(int block_size) { return block_size < kMaxStageRows ? block_size : kMaxStageRows; }
+// Rows of one staged run of a block: the whole block up to kMaxStageRows
+// (16 at head size 256, whose rows are 512 bytes or more); a larger block is
+// staged in runs of that many rows.
+int stage_rows(int block_size, int head_dim) {
+    const int cap = head_dim > 128 ? 16 : kMaxStageRows;
+    return block_size < cap ? block_size : cap;
+}
 
 // Descriptor of one pool seen as a 2-D tensor [rows = NB*Hkv*BS][head_dim],
 // staged in boxes of one 128-byte slab x one run of rows with the 128-byte
@@ -47,7 +51,7 @@ bool encode_pool_map(CUtensorMap *map, void *base, int rows, int head_dim, int b
     const int elem = dtype == PKV_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)head_dim * elem};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)stage_rows(block_size)};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)stage_rows(block_size, head_dim)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, dtype == PKV_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                          : dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -69,7 +73,7 @@ bool valid_geometry(int num_blocks, int block_size, int num_kv_heads, int head_d
     if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 &&
         block_size != 256)
         return false;
-    if (head_dim != 64 && head_dim != 128) return false;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
     return (long long)num_blocks * num_kv_heads * block_size < (1ll << 31);
 }
 
@@ -272,7 +276,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
 
     // The kernel works in staged runs of U rows: a block of BS > 32 rows is
     // 2^unit_shift runs, and partitions (whole blocks) are whole runs.
-    const int BS = pool->block_size, U = stage_rows(BS);
+    const int BS = pool->block_size, U = stage_rows(BS, pool->head_dim);
     int unit_shift = 0;
     while ((U << unit_shift) < BS) ++unit_shift;
     if (((long long)max_blocks_per_seq << unit_shift) >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
@@ -338,12 +342,16 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     L.device = dev;
 
     pkv_status st;
+    const int hd = pool->head_dim;
     if (pool->dtype == PKV_BF16)
-        st = pool->head_dim == 64 ? launch_decode_bf16_d64(L) : launch_decode_bf16_d128(L);
+        st = hd == 64 ? launch_decode_bf16_d64(L)
+                      : (hd == 128 ? launch_decode_bf16_d128(L) : launch_decode_bf16_d256(L));
     else if (pool->dtype == PKV_F16)
-        st = pool->head_dim == 64 ? launch_decode_f16_d64(L) : launch_decode_f16_d128(L);
+        st = hd == 64 ? launch_decode_f16_d64(L)
+                      : (hd == 128 ? launch_decode_f16_d128(L) : launch_decode_f16_d256(L));
     else
-        st = pool->head_dim == 64 ? launch_decode_f32_d64(L) : launch_decode_f32_d128(L);
+        st = hd == 64 ? launch_decode_f32_d64(L)
+                      : (hd == 128 ? launch_decode_f32_d128(L) : PKV_ERR_UNSUPPORTED);
     if (st != PKV_OK || parts <= 1) return st;
     return launch_lse_combine(a, num_seqs, pool->head_dim, U, L.stream);
 }

@@ -195,7 +195,12 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int p = 0; p < kCombDirect; ++p) {
         if (p < P) {
-            if constexpr (PER == 4) {
+            if constexpr (PER == 8) {
+                const float4 x = *reinterpret_cast<const float4 *>(po + (size_t)p * D);
+                const float4 y = *reinterpret_cast<const float4 *>(po + (size_t)p * D + 4);
+                v[p][0] = x.x, v[p][1] = x.y, v[p][2] = x.z, v[p][3] = x.w;
+                v[p][4] = y.x, v[p][5] = y.y, v[p][6] = y.z, v[p][7] = y.w;
+            } else if constexpr (PER == 4) {
                 const float4 x = *reinterpret_cast<const float4 *>(po + (size_t)p * D);
                 v[p][0] = x.x, v[p][1] = x.y, v[p][2] = x.z, v[p][3] = x.w;
             } else {
@@ -295,6 +300,9 @@ pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, i
         const dim3 grid((unsigned)((n + 7) / 8));
         if (head_dim == 64)
             return cuda_status(launch_dependent(lse_combine_kernel<2>, grid, dim3(256), 0, stream, a,
+                                                block_size, (int)n));
+        if (head_dim == 256)
+            return cuda_status(launch_dependent(lse_combine_kernel<8>, grid, dim3(256), 0, stream, a,
                                                 block_size, (int)n));
         return cuda_status(launch_dependent(lse_combine_kernel<4>, grid, dim3(256), 0, stream, a,
                                             block_size, (int)n));

@@ -489,9 +489,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     // Gather this warp's first block numbers before the context length is
     // known (bounded by the table row), so the two dependent loads overlap.
     // (Blocks here are staged runs of BS rows: a pool block of more than 32
-    // rows is 2^ushift runs, all named by its one table entry.  Only the
-    // 32-row instantiation stages such blocks.)
-    const int ushift = BS == kMaxStageRows ? a.unit_shift : 0;
+    // rows (16 at head size 256) is 2^ushift runs, all named by its one table
+    // entry.  Only the 32-row and the head-size-256 instantiations stage such
+    // blocks.)
+    const int ushift = (BS == kMaxStageRows || D == 256) ? a.unit_shift : 0;
     const int b0 = part * a.part_blocks;
     const int tspan = min(a.max_blocks_per_seq << ushift, b0 + a.part_blocks) - b0;
     const int nw_tbl = tspan > warp ? (tspan - warp + NW - 1) / NW : 0;
@@ -663,18 +664,32 @@ pkv_status launch_bs(const DecodeLaunch &L) {
         case 1: return launch_one<T, D, BS, 1, false>(L);
         case 2: return launch_one<T, D, BS, 2, false>(L);
         case 4: return launch_one<T, D, BS, 4, false>(L);
-        case 8: return launch_one<T, D, BS, 8, false>(L);
-        case 16: return launch_one<T, D, BS, 16, false>(L);
-        default: return PKV_ERR_UNSUPPORTED;
+        default: break;
     }
+    if constexpr (D <= 128) {
+        // (head size 256 keeps CUDA-core rows to groups of up to 4: the
+        // tensor-core path takes the larger groups)
+        switch (L.group_pad) {
+            case 8: return launch_one<T, D, BS, 8, false>(L);
+            case 16: return launch_one<T, D, BS, 16, false>(L);
+            default: break;
+        }
+    }
+    return PKV_ERR_UNSUPPORTED;
 }
 
 template <typename T, int D>
 pkv_status launch_d(const DecodeLaunch &L) {
-    switch (L.block_size) {
-        case 16: return launch_bs<T, D, 16>(L);
-        case 32: return launch_bs<T, D, 32>(L);
-        default: return PKV_ERR_UNSUPPORTED;
+    if constexpr (D == 256) {
+        // 512-byte rows: every block is staged in runs of 16 rows
+        if (L.block_size == 16) return launch_bs<T, D, 16>(L);
+        return PKV_ERR_UNSUPPORTED;
+    } else {
+        switch (L.block_size) {
+            case 16: return launch_bs<T, D, 16>(L);
+            case 32: return launch_bs<T, D, 32>(L);
+            default: return PKV_ERR_UNSUPPORTED;
+        }
     }
 }
 

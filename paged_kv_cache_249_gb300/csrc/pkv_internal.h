@@ -130,6 +130,8 @@ pkv_status launch_decode_bf16_d64(const DecodeLaunch &L);
 pkv_status launch_decode_bf16_d128(const DecodeLaunch &L);
 pkv_status launch_decode_f16_d64(const DecodeLaunch &L);
 pkv_status launch_decode_f16_d128(const DecodeLaunch &L);
+pkv_status launch_decode_bf16_d256(const DecodeLaunch &L);
+pkv_status launch_decode_f16_d256(const DecodeLaunch &L);
 
 pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, int block_size,
                               cudaStream_t stream);

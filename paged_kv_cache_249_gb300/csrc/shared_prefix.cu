@@ -398,7 +398,9 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
         (partition_tokens > 0 && partition_tokens % c.BS != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    if (pool->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;  // tensor-core tiles: bf16 or fp16
+    // tensor-core tiles of bf16 or fp16; two 16-row accumulator tiles of a
+    // 256-wide head would not fit a warp's registers
+    if (pool->dtype == PKV_F32 || pool->head_dim > 128) return PKV_ERR_UNSUPPORTED;
     // blocks above kMaxStageRows tokens are staged (and listed) in runs
     c.U = c.BS < kMaxStageRows ? c.BS : kMaxStageRows;
     c.unit_shift = 0;

@@ -247,3 +247,48 @@ def test_f16_output(dtype):
     dw32 = run_decode(w, partition_tokens=128, out_dtype=torch.float32)
     assert torch.equal(dw32.out.to(torch.float16).cpu().view(torch.int16),
                        dw16.out.cpu().view(torch.int16))
+
+
+# ------------------------------------------------------------ head size 256
+
+D256_CASES = [
+    # dtype, BS, H, Hkv
+    ("bf16", 16, 8, 8),
+    ("bf16", 16, 16, 8),
+    ("f16", 16, 16, 4),
+    ("bf16", 64, 32, 4),
+    ("f16", 32, 16, 1),
+]
+
+
+@pytest.mark.parametrize("case", D256_CASES, ids=lambda c: "_".join(map(str, c)))
+def test_head_size_256_matches_oracle(case):
+    """512-byte rows (16-bit pools): blocks are staged in runs of 16 rows;
+    CUDA-core rows for groups up to 4, tensor-core tiles otherwise."""
+    dtype, BS, H, Hkv = case
+    w = _w(dtype, 256, BS, H, Hkv, seed=600 + D256_CASES.index(case))
+    ref, _, _ = oracle_after_write(w)
+    G = H // Hkv
+    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_MMA] + ([pagedkv.PATH_FMA] if G <= 4 else [])
+    for pt in (-1, 0, 2 * BS):
+        for path in paths:
+            dw = run_decode(w, path=path, partition_tokens=pt)
+            assert pagedkv.get_device_error(dw.pool) == 0
+            assert_close(dw.out, ref, dtype, f"{case} path={path} partition={pt}")
+
+
+def test_head_size_256_unsupported_combinations_are_refused():
+    """fp32 pools and CUDA-core rows for groups above 4 are not built at head
+    size 256; the call returns PKV_ERR_UNSUPPORTED and launches nothing."""
+    w32 = _w("f32", 256, 16, 8, 8, ctx=[5, 40], seed=640)
+    dw = pagedkv.DeviceWorkload(w32)
+    with pytest.raises(pagedkv.PagedKVError) as e:
+        dw.decode()
+    assert e.value.status == pagedkv.ERR_UNSUPPORTED
+    w8 = _w("bf16", 256, 16, 16, 2, ctx=[5, 40], seed=641)
+    dw8 = pagedkv.DeviceWorkload(w8)
+    with pytest.raises(pagedkv.PagedKVError) as e:
+        dw8.decode(path=pagedkv.PATH_FMA)
+    assert e.value.status == pagedkv.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw8.pool) == 0
