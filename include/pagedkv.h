@@ -103,10 +103,9 @@ size_t pkv_pool_bytes(int num_blocks, int block_size, int num_kv_heads, int head
  * current device.  dev_error: device int32 error word or NULL.  zero_fill:
  * non-zero clears both pools and the error word on `stream`.
  * Supported: block_size in {16, 32, 64, 128, 256} (the page's range of
- * roughly 16 to 256 tokens; blocks above 32 tokens are staged in runs of 32
+ * roughly 16 to 256 tokens; the kernels stage every block in runs of 16
  * rows); head_dim in {64, 128, 256} (256: the decode takes BF16 or F16
- * pools and stages blocks in runs of 16 rows; the shared-prefix decode takes
- * 64 or 128); dtype F32, BF16 or F16;
+ * pools; the shared-prefix decode takes 64 or 128); dtype F32, BF16 or F16;
  * num_blocks*num_kv_heads*block_size < 2^31.
  */
 pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, int num_kv_heads,

@@ -33,12 +33,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Rows of one staged run of a block: the whole block up to kMaxStageRows
-// (16 at head size 256, whose rows are 512 bytes or more); a larger block is
-// staged in runs of that many rows.
-int stage_rows(int block_size, int head_dim) {
-    const int cap = head_dim > 128 ? 16 : kMaxStageRows;
-    return block_size < cap ? block_size : cap;
+// Rows of one staged run of a block: the whole block up to kMaxStageRows; a
+// larger block is staged in runs of that many rows, so every block size uses
+// the ring geometry tuned for 16-row tiles.
+int stage_rows(int block_size, int /*head_dim*/) {
+    return block_size < kMaxStageRows ? block_size : kMaxStageRows;
 }
 
 // Descriptor of one pool seen as a 2-D tensor [rows = NB*Hkv*BS][head_dim],
@@ -274,7 +273,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     if (cuda_status(cudaGetDevice(&dev)) != PKV_OK) return PKV_ERR_CUDA;
     if (dev != pool->device) return PKV_ERR_INVALID_ARG;
 
-    // The kernel works in staged runs of U rows: a block of BS > 32 rows is
+    // The kernel works in staged runs of U rows: a block of BS > 16 rows is
     // 2^unit_shift runs, and partitions (whole blocks) are whole runs.
     const int BS = pool->block_size, U = stage_rows(BS, pool->head_dim);
     int unit_shift = 0;
@@ -334,6 +333,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     L.num_seqs = num_seqs;
     L.head_dim = pool->head_dim;
     L.block_size = U;
+    L.runs = unit_shift > 0;
     int gp = 1;
     while (gp < group) gp <<= 1;
     L.group_pad = gp;

@@ -466,7 +466,7 @@ struct PathOf<__half, D, BS, GP, true> {
     using type = MmaPath<__half, D, BS, GP>;
 };
 
-template <typename T, int D, int BS, int GP, bool MMA>
+template <typename T, int D, int BS, int GP, bool MMA, bool RUNS>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
@@ -488,11 +488,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     // Gather this warp's first block numbers before the context length is
     // known (bounded by the table row), so the two dependent loads overlap.
-    // (Blocks here are staged runs of BS rows: a pool block of more than 32
-    // rows (16 at head size 256) is 2^ushift runs, all named by its one table
-    // entry.  Only the 32-row and the head-size-256 instantiations stage such
-    // blocks.)
-    const int ushift = (BS == kMaxStageRows || D == 256) ? a.unit_shift : 0;
+    // (Blocks here are staged runs of BS rows: a pool block of more than BS
+    // rows is 2^ushift runs, all named by its one table entry.  Only the RUNS
+    // instantiations stage such blocks; the others compile the shift out.)
+    const int ushift = RUNS ? a.unit_shift : 0;
     const int b0 = part * a.part_blocks;
     const int tspan = min(a.max_blocks_per_seq << ushift, b0 + a.part_blocks) - b0;
     const int nw_tbl = tspan > warp ? (tspan - warp + NW - 1) / NW : 0;
@@ -634,9 +633,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 }
 
 // Explicit-instantiation helper: launch one configuration.
-template <typename T, int D, int BS, int GP, bool MMA>
+template <typename T, int D, int BS, int GP, bool MMA, bool RUNS>
 pkv_status launch_one(const DecodeLaunch &L) {
-    auto kern = paged_decode_kernel<T, D, BS, GP, MMA>;
+    auto kern = paged_decode_kernel<T, D, BS, GP, MMA, RUNS>;
     constexpr int smem = decode_smem_bytes<T, D, BS, GP>();
     static_assert(smem <= 227 * 1024, "shared memory budget");
     // Raise the dynamic shared-memory limit once per device for this kernel.
@@ -653,44 +652,36 @@ pkv_status launch_one(const DecodeLaunch &L) {
         launch_dependent(kern, grid, dim3(kDecodeWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool RUNS>
 pkv_status launch_bs(const DecodeLaunch &L) {
     if constexpr (sizeof(T) == 2) {
         if (L.mma)
-            return L.group_pad <= 8 ? launch_one<T, D, BS, 8, true>(L)
-                                    : launch_one<T, D, BS, 16, true>(L);
+            return L.group_pad <= 8 ? launch_one<T, D, BS, 8, true, RUNS>(L)
+                                    : launch_one<T, D, BS, 16, true, RUNS>(L);
     }
     switch (L.group_pad) {
-        case 1: return launch_one<T, D, BS, 1, false>(L);
-        case 2: return launch_one<T, D, BS, 2, false>(L);
-        case 4: return launch_one<T, D, BS, 4, false>(L);
+        case 1: return launch_one<T, D, BS, 1, false, RUNS>(L);
+        case 2: return launch_one<T, D, BS, 2, false, RUNS>(L);
+        case 4: return launch_one<T, D, BS, 4, false, RUNS>(L);
         default: break;
     }
     if constexpr (D <= 128) {
         // (head size 256 keeps CUDA-core rows to groups of up to 4: the
         // tensor-core path takes the larger groups)
         switch (L.group_pad) {
-            case 8: return launch_one<T, D, BS, 8, false>(L);
-            case 16: return launch_one<T, D, BS, 16, false>(L);
+            case 8: return launch_one<T, D, BS, 8, false, RUNS>(L);
+            case 16: return launch_one<T, D, BS, 16, false, RUNS>(L);
             default: break;
         }
     }
     return PKV_ERR_UNSUPPORTED;
 }
 
+// Every block is staged in runs of 16 rows (a 16-token block is one run).
 template <typename T, int D>
 pkv_status launch_d(const DecodeLaunch &L) {
-    if constexpr (D == 256) {
-        // 512-byte rows: every block is staged in runs of 16 rows
-        if (L.block_size == 16) return launch_bs<T, D, 16>(L);
-        return PKV_ERR_UNSUPPORTED;
-    } else {
-        switch (L.block_size) {
-            case 16: return launch_bs<T, D, 16>(L);
-            case 32: return launch_bs<T, D, 32>(L);
-            default: return PKV_ERR_UNSUPPORTED;
-        }
-    }
+    if (L.block_size != 16) return PKV_ERR_UNSUPPORTED;
+    return L.runs ? launch_bs<T, D, 16, true>(L) : launch_bs<T, D, 16, false>(L);
 }
 
 }  // namespace pkv

@@ -14,7 +14,7 @@ constexpr uint32_t kPoolMagic = 0x504b5631u;  // "PKV1"
 constexpr int kAutoPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 8192;
 constexpr int kMaxGroup = 16;
-constexpr int kMaxStageRows = 32;  // rows of one staged run; larger blocks are staged in runs
+constexpr int kMaxStageRows = 16;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 
 // Arguments of one decode launch; every pointer is a device pointer.
@@ -36,7 +36,7 @@ struct DecodeArgs {
     int num_parts;              // gridDim.z: partitions of the longest allowed context
     int out_dtype;              // pkv_dtype of out
     int contig;                 // 1: contiguous cache, block b of (s, g) is row run (s*Hkv+g)*num_blocks+b
-    int unit_shift;             // a pool block is 2^unit_shift staged runs of BS rows (blocks over 32 rows)
+    int unit_shift;             // a pool block is 2^unit_shift staged runs of BS rows (blocks over 16 rows)
     float scale_log2;           // scale * log2(e)
 };
 
@@ -49,6 +49,7 @@ struct DecodeLaunch {
     int block_size;
     int group_pad;              // FMA path: query rows per CTA (power of two >= group)
     bool mma;
+    bool runs;                  // pool blocks are staged in several runs (unit_shift > 0)
     cudaStream_t stream;
     int device;
 };

@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(kSpWarps * 32)
         return t;
     };
     // physical block of the item's i-th run (chunk of 32, one per lane); a
-    // block of more than 32 tokens is 2^ushift runs, named by one table entry
-    const int ushift = BS == kMaxStageRows ? a.unit_shift : 0;
+    // block of more than 16 tokens is 2^ushift runs, named by one table entry
+    const int ushift = a.unit_shift;
     auto bt_load = [&](const SpItem &t, int chunk) -> int {
         const int i = chunk * 32 + lane;
         if (i >= t.nb) return -1;
@@ -480,13 +480,10 @@ pkv_status launch_sp_one(const SpLaunch &L) {
         launch_dependent(kern, dim3(grid), dim3(kSpWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }
 
+// Every block is staged in runs of 16 rows (a 16-token block is one run).
 template <typename T, int D>
 pkv_status launch_sp_d(const SpLaunch &L) {
-    switch (L.block_size) {
-        case 16: return launch_sp_one<T, D, 16>(L);
-        case 32: return launch_sp_one<T, D, 32>(L);
-        default: return PKV_ERR_UNSUPPORTED;
-    }
+    return L.block_size == 16 ? launch_sp_one<T, D, 16>(L) : PKV_ERR_UNSUPPORTED;
 }
 
 }  // namespace pkv

@@ -148,7 +148,7 @@ LARGE_BLOCK_CASES = [
 @pytest.mark.parametrize("case", LARGE_BLOCK_CASES, ids=lambda c: "_".join(map(str, c)))
 def test_large_blocks_match_oracle(case):
     """Blocks of 64, 128 and 256 tokens (the page's range of roughly 16 to
-    256): the kernel stages each block in runs of 32 rows named by the
+    256): the kernel stages each block in runs of 16 rows named by the
     block's one table entry; contexts end mid-run, mid-block, on a run and on
     a block boundary."""
     dtype, D, BS, H, Hkv = case
@@ -201,7 +201,7 @@ def _reblock(w, BS):
 
 def test_large_blocks_equal_small_blocks_bitwise():
     """The same tokens in blocks of 256 and of 32 give the same bits: the
-    kernel's arithmetic runs over 32-row runs either way, in the same order."""
+    kernel's arithmetic runs over 16-row runs either way, in the same order."""
     w256 = _w("bf16", 128, 256, 32, 8, ctx=[5, 300, 777, 1024], seed=460)
     outs = []
     for w in (w256, _reblock(w256, 32)):

@@ -276,7 +276,7 @@ def test_plan_lists_every_item_once_largest_first(case):
 
 @pytest.mark.parametrize("BS", [64, 128, 256])
 def test_shared_prefix_large_blocks(BS):
-    """Blocks above 32 tokens are listed and staged as 32-row runs; the
+    """Blocks above 16 tokens are listed and staged as 16-row runs; the
     prefix stays whole blocks and the combine checks the tables per block."""
     ctx = _prefix_ctx(2 * BS, [0, 1, 31, 33, BS, BS + 7, 3 * BS])
     groups = [(4, 2 * BS), (3, BS)]
