@@ -42,12 +42,12 @@ FALLBACK_HBM_GBS = 6800.0
 # sources hash to `src`.  Filled in from the profiles summaries.
 NCU_TRAFFIC: dict = {
     # profiles/paged_decode_kernel_mha_7b_gqa_8b_long_ctx.md
-    ("mha_7b", "plain"): {"bytes": 1105864000 + 5669632, "src": "8538972e68c679ea"},
-    ("gqa_8b", "plain"): {"bytes": 2374010000 + 13422848, "src": "8538972e68c679ea"},
-    ("long_ctx", "plain"): {"bytes": 2975505000 + 48528640, "src": "8538972e68c679ea"},
+    ("mha_7b", "plain"): {"bytes": 1105857000 + 5554944, "src": "0dc5653686e8ae90"},
+    ("gqa_8b", "plain"): {"bytes": 2374190000 + 13298176, "src": "0dc5653686e8ae90"},
+    ("long_ctx", "plain"): {"bytes": 2975455000 + 48262912, "src": "0dc5653686e8ae90"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
-    ("shared_prefix", "shared"): {"bytes": 857698816 + 39856896, "src": "c064e8ad5ec2d359"},
+    ("shared_prefix", "shared"): {"bytes": 857754880 + 39394048, "src": "cdf774fffb28d23f"},
 }
 
 
