@@ -533,6 +533,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         const int v1 = __shfl_sync(0xffffffffu, ent1, i & 31);
         return (i >> 5) == cb ? v0 : v1;
     };
+    const uint64_t kv_policy = l2_evict_first_policy();  // K/V tiles are read once
     auto issue = [&](int i, int pb) {
         if (lane == 0) {
             uint64_t *bar = &wbar[i % NST];
@@ -545,8 +546,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                                        : (((pb * a.num_kv_heads + g) << ushift) + run) * BS;
 #pragma unroll
                 for (int sl = 0; sl < Gm::kSlabs; ++sl) {
-                    tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);
-                    tma_load_2d(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar);
+                    tma_load_2d_hint(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar, kv_policy);
+                    tma_load_2d_hint(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar, kv_policy);
                 }
             } else {
                 raise_fault(a.dev_error, PKV_FAULT_BLOCK_ID);

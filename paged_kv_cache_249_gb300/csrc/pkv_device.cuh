@@ -117,6 +117,25 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 // 2-D tiled load of one box at element coordinates (x, y) into shared memory,
 // completing `bar`'s transaction count.  x must be a multiple of 16 bytes /
 // element size (TMA alignment rule); callers pass slab starts (128-byte steps).
+// L2 policy for data read once (K/V tiles): evict first, so that what is
+// read again soon (split partials, queries, tables) stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// The same tiled load with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map, int x,
+                                                 int y, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
     asm volatile(

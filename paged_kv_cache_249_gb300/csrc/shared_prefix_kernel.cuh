@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
         return lane < t.R ? a.nparts[t.seq0 + lane / G] : 0;
     };
     // stage run `run` (of its sequence) of block pb at absolute ring position k
+    const uint64_t kv_policy = l2_evict_first_policy();  // K/V tiles are read once
     auto issue = [&](int g, unsigned k, int pb, int run) {
         if (lane == 0) {
             uint64_t *bar = &wbar[k % NST];
@@ -304,8 +305,8 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 const int y = (((pb * Hkv + g) << ushift) + (run & ((1 << ushift) - 1))) * BS;
 #pragma unroll
                 for (int sl = 0; sl < Gm::kSlabs; ++sl) {
-                    tma_load_2d(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar);
-                    tma_load_2d(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar);
+                    tma_load_2d_hint(dk + sl * Gm::kSlabBytes, &tmk, sl * Gm::kSlabElems, y, bar, kv_policy);
+                    tma_load_2d_hint(dv + sl * Gm::kSlabBytes, &tmv, sl * Gm::kSlabElems, y, bar, kv_policy);
                 }
             } else {
                 raise_fault(a.dev_error, PKV_FAULT_BLOCK_ID);
