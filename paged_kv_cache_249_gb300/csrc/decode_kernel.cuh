@@ -626,8 +626,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             store_out(a.out, oi, res, a.out_dtype);
         } else {
             const size_t pi = (head0 + r) * a.num_parts + part;
-            a.ws_o[pi * D + d] = res;
-            if (d == 0) a.ws_lse[pi] = L > 0.f ? M + __log2f(L) : -CUDART_INF_F;
+            // the combine reads these right after the grid: keep them in L2
+            const uint64_t keep = l2_evict_last_policy();
+            st_f32_hint(a.ws_o + pi * D + d, res, keep);
+            if (d == 0) st_f32_hint(a.ws_lse + pi, L > 0.f ? M + __log2f(L) : -CUDART_INF_F, keep);
         }
     }
     griddep_launch();

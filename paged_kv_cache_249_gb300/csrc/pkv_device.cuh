@@ -125,6 +125,19 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return p;
 }
 
+// L2 policy for data read again soon (split partials): evict last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Stores with an L2 cache policy.
+__device__ __forceinline__ void st_f32_hint(float *ptr, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy)
+                 : "memory");
+}
+
 // The same tiled load with an L2 cache policy.
 __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map, int x,
                                                  int y, uint64_t *bar, uint64_t policy) {
