@@ -42,12 +42,12 @@ FALLBACK_HBM_GBS = 6800.0
 # sources hash to `src`.  Filled in from the profiles summaries.
 NCU_TRAFFIC: dict = {
     # profiles/paged_decode_kernel_mha_7b_gqa_8b_long_ctx.md
-    ("mha_7b", "plain"): {"bytes": 1105857000 + 5554944, "src": "0dc5653686e8ae90"},
-    ("gqa_8b", "plain"): {"bytes": 2374190000 + 13298176, "src": "0dc5653686e8ae90"},
-    ("long_ctx", "plain"): {"bytes": 2975455000 + 48262912, "src": "0dc5653686e8ae90"},
+    ("mha_7b", "plain"): {"bytes": 1105054000 + 3578112, "src": "87cc0cb0df187353"},
+    ("gqa_8b", "plain"): {"bytes": 2369795000 + 3299840, "src": "87cc0cb0df187353"},
+    ("long_ctx", "plain"): {"bytes": 2974808000 + 7462144, "src": "87cc0cb0df187353"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
-    ("shared_prefix", "shared"): {"bytes": 857754880 + 39394048, "src": "cdf774fffb28d23f"},
+    ("shared_prefix", "shared"): {"bytes": 853250304 + 7942656, "src": "148d58404dbba3eb"},
 }
 
 
