@@ -22,7 +22,10 @@
  *     device memory and keeps no mutable global state.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls only enqueue work; nothing synchronises except
- *     pkv_get_device_error.
+ *     pkv_get_device_error.  So every call can be captured in a CUDA graph
+ *     (once its kernels have run eagerly once: their one-time attribute
+ *     set-up is not a stream operation) and replayed with new contents in
+ *     the captured buffers.
  *   - Invalid arguments are rejected on the host with PKV_ERR_INVALID_ARG or
  *     PKV_ERR_UNSUPPORTED before anything is launched.  A failed launch
  *     returns PKV_ERR_CUDA.  No C++ exception crosses this boundary.
