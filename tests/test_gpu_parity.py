@@ -292,3 +292,23 @@ def test_head_size_256_unsupported_combinations_are_refused():
     assert e.value.status == pagedkv.ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert pagedkv.get_device_error(dw8.pool) == 0
+
+
+def test_random_shapes_sweep_wide():
+    """Random shapes over every storage type, block sizes 16-256 and head
+    sizes 64-256 (256 with 16-bit storage), against the oracle."""
+    rng = np.random.default_rng(91)
+    for trial in range(16):
+        dtype = ["f32", "bf16", "f16"][trial % 3]
+        D = int(rng.choice([64, 128] + ([256] if dtype != "f32" else [])))
+        BS = int(rng.choice([16, 32, 64, 128, 256]))
+        Hkv = int(rng.integers(1, 4))
+        G = int(rng.choice([1, 2, 4, 5, 8] if D < 256 else [1, 2, 4, 8]))
+        S = int(rng.integers(1, 7))
+        ctx = rng.integers(0, 1300, size=S).tolist()
+        w = _w(dtype, D, BS, Hkv * G, Hkv, ctx=ctx, seed=700 + trial)
+        ref, _, _ = oracle_after_write(w)
+        pt = int(rng.choice([-1, 0, BS * 2, BS * 4]))
+        dw = run_decode(w, partition_tokens=pt)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, dtype, f"trial {trial}: {dtype} D{D} BS{BS} G{G} ctx {ctx} pt {pt}")

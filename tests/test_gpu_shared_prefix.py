@@ -314,3 +314,31 @@ def test_shared_prefix_f16(case):
         dw = _run(w, 0, out_dtype)
         assert pagedkv.get_device_error(dw.pool) == 0
         assert_close(dw.out, ref, "f16", f"{case} fp16 pools, out {out_dtype}")
+
+
+# ------------------------------------------------------------ random sweep
+
+def test_shared_prefix_random_sweep():
+    """Random group structures, prefix lengths, contexts, partitions, block
+    and head sizes, group sizes and storage types, each against the oracle."""
+    rng = np.random.default_rng(2024)
+    for trial in range(14):
+        BS = int(rng.choice([16, 32, 64]))
+        D = int(rng.choice([64, 128]))
+        Hkv = int(rng.integers(1, 4))
+        G = int(rng.choice([1, 2, 3, 4, 6, 8, 16]))
+        dtype = ["bf16", "f16"][trial % 2]
+        groups, ctx = [], []
+        for _ in range(int(rng.integers(1, 5))):
+            members = int(rng.integers(1, 12))
+            prefix = BS * int(rng.integers(0, 6)) if members > 1 else 0
+            groups.append((members, prefix))
+            ctx += [prefix + int(rng.integers(0, 300)) for _ in range(members)]
+        w = workload.build(f"sweep{trial}", dtype=dtype, context_lens=ctx, num_heads=Hkv * G,
+                           num_kv_heads=Hkv, head_dim=D, block_size=BS, data_seed=9000 + trial,
+                           meta_seed=9100 + trial, groups=groups)
+        ref, _, _ = oracle_after_write(w)
+        pt = int(rng.choice([0, -1, BS, 4 * BS]))
+        dw = _run(w, pt)
+        assert pagedkv.get_device_error(dw.pool) == 0, trial
+        assert_close(dw.out, ref, dtype, f"trial {trial}: BS{BS} D{D} G{G} groups {groups} pt {pt}")
