@@ -21,10 +21,11 @@ from tests.gpu_helpers import assert_close
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("dtype,H,Hkv,BS", [("bf16", 16, 4, 16), ("f32", 8, 8, 32)])
+@pytest.mark.parametrize("dtype,H,Hkv,BS", [("bf16", 16, 4, 16), ("f32", 8, 8, 32),
+                                             ("f16", 16, 2, 64)])
 def test_manager_driven_decode_loop(dtype, H, Hkv, BS):
     D, NB, MB = 128, 160, 24
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[dtype]
     gen = torch.Generator().manual_seed(1234)
     rnd = lambda *shape: torch.randn(*shape, generator=gen).to(tdt)  # noqa: E731
 
@@ -94,7 +95,7 @@ def test_manager_driven_decode_loop(dtype, H, Hkv, BS):
         assert pagedkv.get_device_error(pool) == 0
         ref = oracle.paged_decode(q, k_host, v_host, bt_host, cl, scale)
         assert_close(out, ref, dtype, f"step {step}")
-    view = torch.int16 if dtype == "bf16" else torch.int32
+    view = torch.int32 if dtype == "f32" else torch.int16
     assert torch.equal(k_dev.cpu().view(view), k_host.view(view))
     assert torch.equal(v_dev.cpu().view(view), v_host.view(view))
 
