@@ -207,14 +207,16 @@ pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const vo
 
 // 0 = automatic.  Partitions cost one CTA start-up each (block-table and
 // first-tile latency), so take the longest partition (2048, 1024 or 512
-// tokens) that still gives about nine waves of CTAs (three resident per SM);
-// no split when the whole context fits in one partition.  `units` is
-// num_seqs * num_kv_heads; sms <= 0 sizes for the smallest automatic choice.
-static int resolve_partition(int partition_tokens, int max_context_len, long long units, int sms) {
+// tokens) that still gives about nine waves of CTAs (ctas_per_sm resident
+// per SM); no split when the whole context fits in one partition.  `units`
+// is num_seqs * num_kv_heads; sms <= 0 sizes for the smallest automatic
+// choice.
+static int resolve_partition(int partition_tokens, int max_context_len, long long units, int sms,
+                             int ctas_per_sm = 3) {
     if (partition_tokens != 0) return partition_tokens;
     if (max_context_len <= kAutoPartitionTokens) return -1;
     if (sms <= 0) return kAutoPartitionTokens;
-    const long long target = 9ll * 3 * sms;
+    const long long target = 9ll * ctas_per_sm * sms;
     for (int pt = 2048; pt > kAutoPartitionTokens; pt /= 2)
         if (units * ((max_context_len + pt - 1) / pt) >= target) return pt;
     return kAutoPartitionTokens;
@@ -301,8 +303,11 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     a.unit_shift = unit_shift;
     a.scale_log2 = scale * 1.4426950408889634f;
 
+    // the tensor-core kernel of a 256-wide head holds 254 registers a thread:
+    // two CTAs per SM instead of three
+    const int ctas_per_sm = (pool->head_dim == 256 && mma) ? 2 : 3;
     const int pt = resolve_partition(partition_tokens, ctx_cap, (long long)num_seqs * num_kv_heads,
-                                     sm_count(dev));
+                                     sm_count(dev), ctas_per_sm);
     int parts = 1;
     if (pt > 0) {
         a.part_blocks = pt / U;
