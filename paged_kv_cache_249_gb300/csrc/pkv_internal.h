@@ -20,7 +20,7 @@ constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work ite
 // Arguments of one decode launch; every pointer is a device pointer.
 struct DecodeArgs {
     const void *q;              // [S][H][D] pool dtype
-    void *out;                  // [S][H][D] fp32 or bf16
+    void *out;                  // [S][H][D] in out_dtype (fp32, bf16 or fp16)
     float *ws_o;                // [S][H][P][D] normalised partition outputs (split only)
     float *ws_lse;              // [S][H][P] log2-sum-exp of each partition (split only)
     const int32_t *block_tables;
@@ -32,7 +32,7 @@ struct DecodeArgs {
     int max_blocks_per_seq;
     int num_blocks;
     int ctx_cap;                // min(max_blocks_per_seq * BS, max_context_len)
-    int part_blocks;            // KV blocks per partition (one CTA each)
+    int part_blocks;            // staged runs per partition (one CTA each)
     int num_parts;              // gridDim.z: partitions of the longest allowed context
     int out_dtype;              // pkv_dtype of out
     int contig;                 // 1: contiguous cache, block b of (s, g) is row run (s*Hkv+g)*num_blocks+b
@@ -46,7 +46,7 @@ struct DecodeLaunch {
     DecodeArgs args;
     int num_seqs;
     int head_dim;
-    int block_size;
+    int block_size;             // rows of a staged run (16)
     int group_pad;              // FMA path: query rows per CTA (power of two >= group)
     bool mma;
     bool runs;                  // pool blocks are staged in several runs (unit_shift > 0)
@@ -69,7 +69,7 @@ static_assert(sizeof(SpEntry) == 32, "work item is two 16-byte words");
 // Arguments of the persistent shared-prefix decode kernel.
 struct SpArgs {
     const void *q;              // [S][H][D] bf16
-    void *out;                  // [S][H][D] fp32 or bf16
+    void *out;                  // [S][H][D] in out_dtype (fp32, bf16 or fp16)
     float *ws_o;                // [S][H][num_slots][D] partial outputs
     float *ws_lse;              // [S][H][num_slots] their log2-sum-exp
     const int32_t *block_tables;
