@@ -20,9 +20,9 @@ Recipe (all draws from NumPy PCG64):
     K pool, V pool, new key, new value); each tensor is filled in chunks of
     2**24 float32 N(0,1) draws, chunk i from its own grandchild stream, so
     the values do not depend on the thread count;
-  * bf16 workloads round those float32 draws to bf16 with round-to-nearest-
-    even (``torch.Tensor.to(torch.bfloat16)``); both sides see the rounded
-    values.
+  * bf16 (and fp16) workloads round those float32 draws to bf16 (fp16)
+    with round-to-nearest-even (``torch.Tensor.to``); both sides see the
+    rounded values.
 
 Layout (our choice, 16-byte aligned rows): K pool and V pool are separate
 ``[num_blocks][num_kv_heads][block_size][head_dim]`` tensors.
