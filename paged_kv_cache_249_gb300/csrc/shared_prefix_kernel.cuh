@@ -115,17 +115,19 @@ struct SpMma {
                     ldsm_x4(qaddr + swz_offset<QR>(qrow, (2 * kc + h) * 2 + (lane >> 4)),
                             qa[t][h][0], qa[t][h][1], qa[t][h][2], qa[t][h][3]);
             }
+            uint32_t kb[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kaddr + swz_offset<BS>(r0 + nt * 8 + (lane & 7), kc * 4 + (lane >> 3)), b0,
-                        b1, b2, b3);
+            for (int nt = 0; nt < 2; ++nt)
+                ldsm_x4(kaddr + swz_offset<BS>(r0 + nt * 8 + (lane & 7), kc * 4 + (lane >> 3)),
+                        kb[nt][0], kb[nt][1], kb[nt][2], kb[nt][3]);
+            // consecutive MMAs update different accumulators (no back-to-back chain)
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    MM::mma(s[t][nt], qa[t][0], b0, b1);
-                    MM::mma(s[t][nt], qa[t][1], b2, b3);
-                }
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int t = 0; t < MT; ++t)
+                        MM::mma(s[t][nt], qa[t][h], kb[nt][2 * h], kb[nt][2 * h + 1]);
         }
         // online softmax per row (log2 domain)
         uint32_t ph[MT][4], pl[MT][4];
@@ -202,8 +204,11 @@ struct SpMma {
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 MM::mma(o[t][2 * np], ph[t], b0, b1);
-                MM::mma(o[t][2 * np], pl[t], b0, b1);
                 MM::mma(o[t][2 * np + 1], ph[t], b2, b3);
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                MM::mma(o[t][2 * np], pl[t], b0, b1);
                 MM::mma(o[t][2 * np + 1], pl[t], b2, b3);
             }
         }
