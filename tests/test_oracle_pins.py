@@ -332,3 +332,31 @@ def test_fp16_matches_brute_force():
     ref = _brute.paged_decode(w.q.numpy(), w.k_pool.numpy(), w.v_pool.numpy(), w.block_tables,
                               w.context_lens, w.scale)
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_block_size_does_not_change_the_result():
+    """The same tokens laid out in blocks of 16, 64 and 256 tokens (the
+    page's range of roughly 16 to 256) give bit-identical oracle outputs:
+    paging is storage, not arithmetic."""
+    w = workload.build("pin_bs", dtype="bf16", context_lens=[1, 255, 256, 257, 700],
+                       num_heads=8, num_kv_heads=2, head_dim=64, block_size=16, data_seed=61,
+                       meta_seed=62)
+    outs = []
+    for BS in (16, 64, 256):
+        S, Hkv, D = w.num_seqs, w.num_kv_heads, w.head_dim
+        nblk = [-(-int(c) // BS) for c in w.context_lens]
+        k = torch.zeros((sum(nblk), Hkv, BS, D), dtype=w.k_pool.dtype)
+        v = torch.zeros_like(k)
+        bt = np.full((S, max(nblk)), -1, dtype=np.int32)
+        order = np.random.default_rng(BS).permutation(sum(nblk))  # scattered placement
+        nxt = 0
+        for s in range(S):
+            for b in range(nblk[s]):
+                bt[s, b] = order[nxt]
+                for j in range(b * BS, min(int(w.context_lens[s]), (b + 1) * BS)):
+                    src = int(w.block_tables[s, j // w.block_size]), j % w.block_size
+                    k[order[nxt], :, j % BS] = w.k_pool[src[0], :, src[1]]
+                    v[order[nxt], :, j % BS] = w.v_pool[src[0], :, src[1]]
+                nxt += 1
+        outs.append(oracle.paged_decode(w.q, k, v, bt, w.context_lens, w.scale, num_threads=2))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
