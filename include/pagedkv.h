@@ -135,7 +135,11 @@ pkv_status pkv_block_table_upload(int32_t *dev_block_tables, const int32_t *host
  * h.  key/value: device [num_tokens][num_kv_heads][head_dim], pool dtype,
  * contiguous.  slot_mapping: device int64 [num_tokens].  A negative slot is
  * padding and skipped; a slot >= num_blocks*block_size sets PKV_FAULT_SLOT
- * and is skipped.  Bytes are copied exactly.
+ * and is skipped.  Bytes are copied exactly.  The non-negative slots of one
+ * call must be distinct: if two tokens name one slot, which of them lands
+ * there is not specified.  (A sequence whose new token falls inside a block
+ * it shares must be given its own copy of that block first; see
+ * pkv_copy_blocks and the block manager.)
  */
 pkv_status pkv_reshape_and_cache(const pkv_pool *pool, const void *key, const void *value,
                                  const int64_t *slot_mapping, int num_tokens, void *stream);

@@ -312,3 +312,15 @@ def test_random_shapes_sweep_wide():
         dw = run_decode(w, partition_tokens=pt)
         assert pagedkv.get_device_error(dw.pool) == 0
         assert_close(dw.out, ref, dtype, f"trial {trial}: {dtype} D{D} BS{BS} G{G} ctx {ctx} pt {pt}")
+
+
+def test_largest_batch_of_sequences():
+    """num_seqs at its bound (65535, the grid's y extent), short ragged
+    contexts including empty ones; every sequence against the oracle."""
+    S = 65535
+    ctx = np.random.default_rng(77).integers(0, 41, size=S).tolist()
+    w = _w("bf16", 64, 16, 4, 2, ctx=ctx, seed=880)
+    ref, _, _ = oracle_after_write(w)
+    dw = run_decode(w, partition_tokens=0)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "bf16", "65535 sequences")

@@ -333,7 +333,11 @@ def test_shared_prefix_random_sweep():
             members = int(rng.integers(1, 12))
             prefix = BS * int(rng.integers(0, 6)) if members > 1 else 0
             groups.append((members, prefix))
-            ctx += [prefix + int(rng.integers(0, 300)) for _ in range(members)]
+            # at most one member ends on the prefix: its new token is written
+            # into the shared block, and two such writers would race on a slot
+            own = [int(rng.integers(1, 300)) for _ in range(members)]
+            own[0] = int(rng.integers(0, 300))
+            ctx += [prefix + o for o in own]
         w = workload.build(f"sweep{trial}", dtype=dtype, context_lens=ctx, num_heads=Hkv * G,
                            num_kv_heads=Hkv, head_dim=D, block_size=BS, data_seed=9000 + trial,
                            meta_seed=9100 + trial, groups=groups)
@@ -342,3 +346,24 @@ def test_shared_prefix_random_sweep():
         dw = _run(w, pt)
         assert pagedkv.get_device_error(dw.pool) == 0, trial
         assert_close(dw.out, ref, dtype, f"trial {trial}: BS{BS} D{D} G{G} groups {groups} pt {pt}")
+
+
+def test_more_sequences_than_the_plan_stages():
+    """Above 8192 sequences the planning kernel reads context lengths from
+    global memory instead of staging them in shared memory."""
+    rng = np.random.default_rng(31)
+    groups, ctx = [], []
+    while len(ctx) < 9000:
+        members = int(rng.integers(1, 5))
+        prefix = 16 * int(rng.integers(1, 4)) if members > 1 else 0
+        groups.append((members, prefix))
+        # every member's new token lies past the shared prefix (two members
+        # ending on the prefix would write the same shared slot)
+        ctx += [prefix + int(rng.integers(1, 40)) for _ in range(members)]
+    w = workload.build("many", dtype="bf16", context_lens=ctx, num_heads=8, num_kv_heads=2,
+                       head_dim=64, block_size=16, data_seed=4242, meta_seed=4343, groups=groups)
+    assert w.num_seqs > 8192
+    ref, _, _ = oracle_after_write(w)
+    dw = _run(w, 0)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "bf16", f"{w.num_seqs} sequences")
