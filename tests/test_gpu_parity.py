@@ -324,3 +324,13 @@ def test_largest_batch_of_sequences():
     dw = run_decode(w, partition_tokens=0)
     assert pagedkv.get_device_error(dw.pool) == 0
     assert_close(dw.out, ref, "bf16", "65535 sequences")
+
+
+def test_more_partitions_than_one_weight_chunk():
+    """A 600k-token context in 512-token partitions (1172 parts) takes the
+    many-part combine through more than one 1024-part chunk of weights."""
+    w = _w("bf16", 64, 16, 4, 1, ctx=[600_000, 3, 70_000], seed=890)
+    ref, _, _ = oracle_after_write(w)
+    dw = run_decode(w, partition_tokens=512)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "bf16", "1172 partitions")

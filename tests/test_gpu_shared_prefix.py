@@ -367,3 +367,14 @@ def test_more_sequences_than_the_plan_stages():
     dw = _run(w, 0)
     assert pagedkv.get_device_error(dw.pool) == 0
     assert_close(dw.out, ref, "bf16", f"{w.num_seqs} sequences")
+
+
+def test_more_than_32_parts_per_sequence():
+    """A 4096-token prefix in 64-token parts gives every member more than 32
+    partials: the combine walks its weights 32 at a time."""
+    ctx = _prefix_ctx(4096, [1, 50, 700, 1500])
+    w = _w("many_parts", ctx, [(4, 4096)], 16, 4, 128, 16, seed=77)
+    ref, _, _ = oracle_after_write(w)
+    dw = _run(w, 64)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, "bf16", "64-token parts")
