@@ -13,10 +13,12 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("partition", [-1, 0, 256])
-@pytest.mark.parametrize("dtype,H,Hkv", [("bf16", 32, 8), ("bf16", 16, 16), ("f32", 8, 2)])
-def test_contiguous_equals_paged_bitwise(dtype, H, Hkv, partition):
+@pytest.mark.parametrize("dtype,H,Hkv,D", [("bf16", 32, 8, 128), ("bf16", 16, 16, 128),
+                                           ("f32", 8, 2, 128), ("f16", 32, 8, 128),
+                                           ("bf16", 16, 4, 256)])
+def test_contiguous_equals_paged_bitwise(dtype, H, Hkv, D, partition):
     w = workload.build("contig", dtype=dtype, context_lens=[1, 300, 17, 1024, 511], num_heads=H,
-                       num_kv_heads=Hkv, head_dim=128, block_size=16, data_seed=3, meta_seed=4)
+                       num_kv_heads=Hkv, head_dim=D, block_size=16, data_seed=3, meta_seed=4)
     dw = pagedkv.DeviceWorkload(w, partition_tokens=partition)
     dw.step()
     cache = pagedkv.ContiguousCache.from_paged(w, k_pool=dw.k_pool, v_pool=dw.v_pool)

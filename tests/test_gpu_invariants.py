@@ -36,11 +36,13 @@ def _replace(w, placement_seed):
                                num_blocks=NB2)
 
 
-@pytest.mark.parametrize("dtype,H,Hkv", [("bf16", 32, 8), ("bf16", 16, 16), ("f32", 8, 2)])
+@pytest.mark.parametrize("dtype,H,Hkv,BS", [("bf16", 32, 8, 16), ("bf16", 16, 16, 16),
+                                            ("f32", 8, 2, 16), ("f16", 32, 8, 16),
+                                            ("bf16", 32, 8, 64)])
 @pytest.mark.parametrize("partition", [-1, 256])
-def test_placement_invariance_bitwise(dtype, H, Hkv, partition):
+def test_placement_invariance_bitwise(dtype, H, Hkv, BS, partition):
     w = workload.build("perm", dtype=dtype, context_lens=[3, 200, 1000, 47, 512], num_heads=H,
-                       num_kv_heads=Hkv, head_dim=128, block_size=16, data_seed=11, meta_seed=12)
+                       num_kv_heads=Hkv, head_dim=128, block_size=BS, data_seed=11, meta_seed=12)
     base = run_decode(w, partition_tokens=partition).out.cpu()
     for seed in (1, 2):
         other = run_decode(_replace(w, seed), partition_tokens=partition).out.cpu()
