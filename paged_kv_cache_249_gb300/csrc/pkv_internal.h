@@ -85,7 +85,7 @@ struct SpArgs {
     int suffix_base;
     int num_seqs;
     int block_size;             // tokens per pool block
-    int unit_shift;             // a block is 2^unit_shift staged runs (blocks over 32 tokens);
+    int unit_shift;             // a block is 2^unit_shift staged runs (blocks over 16 tokens);
                                 // work items count runs
     int num_heads;
     int num_kv_heads;

@@ -80,7 +80,7 @@ struct SpPlan {
     int ctx_cap;            // context lengths are clamped to [0, ctx_cap]
     int max_prefix_len;     // tokens (already capped by max_context_len)
     int block_size;         // tokens per pool block (a shared prefix is whole blocks)
-    int run_rows;           // tokens per staged run (min(block_size, 32)); the work list counts runs
+    int run_rows;           // tokens per staged run (min(block_size, 16)); the work list counts runs
     int pbp, pbs;           // blocks per prefix / suffix item
     int cls_shift_p, cls_shift_s;  // size classes: (pbp - nb) >> cls_shift_p, likewise suffix
     int members_per_item;   // floor(32 / group)
@@ -101,17 +101,25 @@ __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c
 constexpr int kPlanClasses = 64;
 constexpr int kPlanSmemSeqs = 8192;
 
-// One CTA turns the group description into the work list.  A group with a
+// A group as a planning warp sees it (warp-uniform).
+struct PlanGroup {
+    int start, end;  // members [start, end)
+    int pblk;        // shared runs (0 = nothing shared)
+};
+
+// One CTA turns the group description into the work list; each warp takes
+// whole groups, its lanes the group's members and items.  A group with a
 // shared prefix gets ceil(members / members_per_item) x ceil(prefix blocks /
 // pbp) prefix items; every sequence gets ceil(own blocks / pbs) suffix items.
 // Prefix items (the largest) and suffix items go to separate regions, and the
-// decode kernel takes all prefix items first.  The first pass over the groups
-// checks each description and counts the items of every size class; after a
-// scan of the class counts, the second pass writes each item at the next
-// free entry of its class.  All inputs are read in one parallel round trip
-// (context lengths into shared memory, a thread's own group into registers),
-// so the passes touch no global memory but the work list.
+// decode kernel takes all prefix items first.  The first pass checks each
+// description and counts the items of every size class; after a scan of the
+// class counts, the second pass reserves, per group, one range of entries
+// for its full-size items and one entry in the right class for each ragged
+// item, so no lane waits on more than two atomics in a row.  Context lengths
+// are read once, into shared memory.
 __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(const SpPlan p) {
+    constexpr unsigned FULL = 0xffffffffu;
     __shared__ int s_ctx[kPlanSmemSeqs];
     __shared__ int s_cls[2][kPlanClasses];  // items per class, then the next free entry
     __shared__ int s_tot[2];
@@ -119,33 +127,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     // griddepcontrol.wait before it reads anything written here
     griddep_launch();
     griddep_wait();  // inputs written by the kernel before this one are complete
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     if (tid < 2 * kPlanClasses) (&s_cls[0][0])[tid] = 0;
     const bool staged = p.num_seqs <= kPlanSmemSeqs;
     bool bad = false;
-    int my_start = 0, my_end = 0, my_plen = 0;  // group tid (when tid < num_groups)
     for (int i = tid; i <= p.num_groups || i < p.num_seqs; i += blockDim.x) {
-        int v = 0, vn = 0, pl = 0, c = 0;
-        if (i <= p.num_groups) v = __ldg(p.group_starts + i);
-        if (i < p.num_groups) {
-            vn = __ldg(p.group_starts + i + 1);
-            pl = __ldg(p.prefix_lens + i);
-        }
-        if (i < p.num_seqs) c = __ldg(p.context_lens + i);
         if (i <= p.num_groups) {
+            const int v = __ldg(p.group_starts + i);
             if (v < 0 || v > p.num_seqs) bad = true;
             if (i == 0 && v != 0) bad = true;
             if (i == p.num_groups && v != p.num_seqs) bad = true;
-            if (i < p.num_groups && v > vn) bad = true;
+            if (i < p.num_groups && v > __ldg(p.group_starts + i + 1)) bad = true;
         }
         if (i < p.num_seqs) {
+            const int c = __ldg(p.context_lens + i);
             if (c < 0 || c > p.ctx_cap) raise_fault(p.dev_error, PKV_FAULT_CONTEXT);
             if (staged) s_ctx[i] = clamp_ctx(c, p.ctx_cap);
-        }
-        if (i == tid) {
-            my_start = v;
-            my_end = vn;
-            my_plen = pl;
         }
     }
     const bool flat = __syncthreads_or(bad);
@@ -156,68 +153,69 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     const int ngr = flat ? p.num_seqs : p.num_groups;
     const int BS = p.run_rows, mpi = p.members_per_item;
 
-    // members [start, end) of group i and the blocks they share (0 = none);
-    // a description that breaks the rules shares nothing (and is reported)
-    auto group_of = [&](int i, int &start, int &end) -> int {
-        if (flat) {
-            start = i;
-            end = i + 1;
-            return 0;
-        }
-        int plen;
-        if (i == tid) {
-            start = my_start;
-            end = my_end;
-            plen = my_plen;
-        } else {
-            start = __ldg(p.group_starts + i);
-            end = __ldg(p.group_starts + i + 1);
-            plen = __ldg(p.prefix_lens + i);
-        }
-        if (plen == 0) return 0;
-        bool ok = plen > 0 && plen % p.block_size == 0 && plen <= p.max_prefix_len;
-        for (int s = start; ok && s < end; ++s) ok = plen <= ctx_of(s);
+    // members of group gi and the runs they share; a description that breaks
+    // the rules shares nothing (and is reported)
+    auto group_of = [&](int gi) -> PlanGroup {
+        PlanGroup G{gi, gi + 1, 0};
+        if (flat) return G;
+        G.start = __ldg(p.group_starts + gi);
+        G.end = __ldg(p.group_starts + gi + 1);
+        const int plen = __ldg(p.prefix_lens + gi);
+        if (plen == 0) return G;
+        bool fits = true;
+        for (int s = G.start + lane; s < G.end; s += 32) fits &= plen <= ctx_of(s);
+        const bool ok = __all_sync(FULL, fits) && plen > 0 && plen % p.block_size == 0 &&
+                        plen <= p.max_prefix_len;
         if (!ok) {
-            raise_fault(p.dev_error, PKV_FAULT_PREFIX);
-            return 0;
+            if (lane == 0) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
+            return G;
         }
-        return end - start >= 2 ? plen / BS : 0;  // one member: nothing to share
+        if (G.end - G.start >= 2) G.pblk = plen / BS;  // one member: nothing to share
+        return G;
     };
     auto cls_p = [&](int nb) { return (p.pbp - nb) >> p.cls_shift_p; };
     auto cls_s = [&](int nb) { return (p.pbs - nb) >> p.cls_shift_s; };
+    // suffix items of sequence s (nq; the last one has `last` runs)
+    auto suffix_of = [&](int s, int pblk, int &ctx, int &nb, int &last) -> int {
+        ctx = ctx_of(s);
+        nb = (ctx + BS - 1) / BS;
+        const int own = nb - pblk;
+        if (own <= 0) return 0;
+        const int nq = (own + p.pbs - 1) / p.pbs;
+        last = own - (nq - 1) * p.pbs;
+        return nq;
+    };
 
     // pass 1: items per size class
-    int my_pblk = 0;  // group tid's shared blocks, for pass 2
 #pragma unroll 1
-    for (int i = tid; i < ngr; i += blockDim.x) {
-        int start, end;
-        const int pblk = group_of(i, start, end);
-        if (i == tid) my_pblk = pblk;
-        if (pblk > 0) {
-            const int pp = (pblk + p.pbp - 1) / p.pbp;
-            const int sets = (end - start + mpi - 1) / mpi;
+    for (int gi = warp; gi < ngr; gi += nwarps) {
+        const PlanGroup G = group_of(gi);
+        if (G.pblk > 0 && lane == 0) {
+            const int pp = (G.pblk + p.pbp - 1) / p.pbp;
+            const int sets = (G.end - G.start + mpi - 1) / mpi;
             if (pp > 1) atomicAdd(&s_cls[0][0], sets * (pp - 1));
-            atomicAdd(&s_cls[0][cls_p(pblk - (pp - 1) * p.pbp)], sets);
+            atomicAdd(&s_cls[0][cls_p(G.pblk - (pp - 1) * p.pbp)], sets);
         }
         int full = 0;
-        for (int s = start; s < end; ++s) {
-            const int own = (ctx_of(s) + BS - 1) / BS - pblk;
-            if (own <= 0) continue;
-            const int nq = (own + p.pbs - 1) / p.pbs;
+        for (int s = G.start + lane; s < G.end; s += 32) {
+            int ctx, nb, last;
+            const int nq = suffix_of(s, G.pblk, ctx, nb, last);
+            if (nq == 0) continue;
             full += nq - 1;
-            atomicAdd(&s_cls[1][cls_s(own - (nq - 1) * p.pbs)], 1);
+            atomicAdd(&s_cls[1][cls_s(last)], 1);
         }
-        if (full > 0) atomicAdd(&s_cls[1][0], full);
+        full = __reduce_add_sync(FULL, full);
+        if (full > 0 && lane == 0) atomicAdd(&s_cls[1][0], full);
     }
     __syncthreads();
     // exclusive scan of the class counts: warp r for region r
     if (tid < 64) {
-        const int r = tid >> 5, lane = tid & 31;
+        const int r = tid >> 5;
         const int c0 = s_cls[r][2 * lane], c1 = s_cls[r][2 * lane + 1];
         int inc = c0 + c1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, inc, off);
+            const int x = __shfl_up_sync(FULL, inc, off);
             if (lane >= off) inc += x;
         }
         const int ex = inc - c0 - c1;
@@ -227,46 +225,64 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     }
     __syncthreads();
 
-    // pass 2: every item at the next free entry of its class
+    // pass 2: every item at a free entry of its class
 #pragma unroll 1
-    for (int i = tid; i < ngr; i += blockDim.x) {
-        int start, end, pblk;
-        if (i == tid) {
-            pblk = my_pblk;
-            start = flat ? i : my_start;
-            end = flat ? i + 1 : my_end;
-        } else {
-            pblk = group_of(i, start, end);
-        }
-        const int pp = (pblk + p.pbp - 1) / p.pbp;
-        for (int m0 = start; m0 < end && pp > 0; m0 += mpi) {
-            const int nm = min(mpi, end - m0);
-            for (int q = 0; q < pp; ++q) {
-                const int b0 = q * p.pbp, b1 = min(pblk, b0 + p.pbp);
-                const int e = atomicAdd(&s_cls[0][cls_p(b1 - b0)], 1);
+    for (int gi = warp; gi < ngr; gi += nwarps) {
+        const PlanGroup G = group_of(gi);
+        const int pp = (G.pblk + p.pbp - 1) / p.pbp;
+        if (pp > 0) {
+            // item k of the group: member set k / pp, part k % pp; the full
+            // parts of all sets take one range, the last parts another
+            const int sets = (G.end - G.start + mpi - 1) / mpi;
+            int bf = 0, br = 0;
+            if (lane == 0) {
+                if (pp > 1) bf = atomicAdd(&s_cls[0][0], sets * (pp - 1));
+                br = atomicAdd(&s_cls[0][cls_p(G.pblk - (pp - 1) * p.pbp)], sets);
+            }
+            bf = __shfl_sync(FULL, bf, 0);
+            br = __shfl_sync(FULL, br, 0);
+            for (int k = lane; k < sets * pp; k += 32) {
+                const int set = k / pp, q = k - set * pp;
+                const int e = q < pp - 1 ? bf + set * (pp - 1) + q : br + set;
                 if (e >= p.prefix_cap) {
                     raise_fault(p.dev_error, PKV_FAULT_PREFIX);
                     continue;
                 }
-                p.entries[e] = SpEntry{m0, nm, start, b0, b1, q, b1 * BS, 0};
+                const int m0 = G.start + set * mpi, b0 = q * p.pbp, b1 = min(G.pblk, b0 + p.pbp);
+                p.entries[e] = SpEntry{m0, min(mpi, G.end - m0), G.start, b0, b1, q, b1 * BS, 0};
             }
         }
-        for (int s = start; s < end; ++s) {
-            const int ctx = ctx_of(s);
-            const int nb = (ctx + BS - 1) / BS;
-            int nq = 0;
-            for (int b0 = pblk; b0 < nb; b0 += p.pbs, ++nq) {
-                const int b1 = min(nb, b0 + p.pbs);
-                const int f = atomicAdd(&s_cls[1][cls_s(b1 - b0)], 1);
+        for (int s0 = G.start; s0 < G.end; s0 += 32) {
+            const int s = s0 + lane;
+            int ctx = 0, nb = 0, last = 0, nq = 0;
+            if (s < G.end) nq = suffix_of(s, G.pblk, ctx, nb, last);
+            // full items: one range for the warp, split by an exclusive scan
+            const int nf = nq > 0 ? nq - 1 : 0;
+            int inc = nf;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int x = __shfl_up_sync(FULL, inc, off);
+                if (lane >= off) inc += x;
+            }
+            const int tot = __shfl_sync(FULL, inc, 31);
+            int base = 0;
+            if (lane == 0 && tot > 0) base = atomicAdd(&s_cls[1][0], tot);
+            base = __shfl_sync(FULL, base, 0) + inc - nf;
+            const int fr = nq > 0 ? atomicAdd(&s_cls[1][cls_s(last)], 1) : 0;
+            for (int q = 0; q < nq; ++q) {
+                const int f = q < nq - 1 ? base + q : fr;
                 if (f >= p.suffix_cap) {
                     raise_fault(p.dev_error, PKV_FAULT_PREFIX);
                     continue;
                 }
-                p.entries[p.prefix_cap + f] = SpEntry{s, 1, s, b0, b1, pp + nq, ctx, 0};
+                const int b0 = G.pblk + q * p.pbs, b1 = min(nb, b0 + p.pbs);
+                p.entries[p.prefix_cap + f] = SpEntry{s, 1, s, b0, b1, pp + q, ctx, 0};
             }
-            p.nparts[s] = pp + nq;
-            p.share[2 * s] = start;
-            p.share[2 * s + 1] = pblk;
+            if (s < G.end) {
+                p.nparts[s] = pp + nq;
+                p.share[2 * s] = G.start;
+                p.share[2 * s + 1] = G.pblk;
+            }
         }
     }
     if (tid == 0) {

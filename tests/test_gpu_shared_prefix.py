@@ -40,6 +40,20 @@ def _prefix_ctx(prefix, suffixes):
     return [prefix + s for s in suffixes]
 
 
+def _varied_groups(n_groups=70, seed=2024):
+    """More groups than the planning CTA has warps: one to four members each,
+    prefixes of 0 to 5 whole blocks, every member with at least one own token
+    (so no two members write into a shared block)."""
+    rng = np.random.default_rng(seed)
+    ctx, groups = [], []
+    for _ in range(n_groups):
+        m = int(rng.choice([1, 1, 2, 3, 4]))
+        pre = int(rng.choice([0, 16, 32, 64, 80]))
+        ctx += [pre + int(x) for x in rng.integers(1, 150, size=m)]
+        groups.append((m, pre))
+    return ctx, groups
+
+
 CASES = {
     # name: (context lengths, groups, H, Hkv, D, BS)
     "g4_eight_members": (_prefix_ctx(256, [0, 1, 15, 16, 17, 100, 300, 700]), [(8, 256)],
@@ -54,6 +68,7 @@ CASES = {
     "d128_bs32": (_prefix_ctx(640, [31, 32, 33, 500]), [(4, 640)], 16, 4, 128, 32),
     "d64_bs16_mha": (_prefix_ctx(48, [1, 2, 3]), [(3, 48)], 4, 4, 64, 16),
     "big_group": (_prefix_ctx(1024, list(range(1, 40 * 7, 7))), [(40, 1024)], 8, 8, 128, 16),
+    "varied_groups": (*_varied_groups(), 8, 2, 128, 16),
 }
 
 
@@ -237,7 +252,7 @@ def _expected_items(w, pbp, pbs):
     return pre, suf
 
 
-@pytest.mark.parametrize("case", ["g4_ragged_groups", "big_group", "g3_odd"])
+@pytest.mark.parametrize("case", ["g4_ragged_groups", "big_group", "g3_odd", "varied_groups"])
 def test_plan_lists_every_item_once_largest_first(case):
     """The plan's entries are exactly the items of the description, each
     region (prefix items, then suffix items) in non-increasing block count, so
