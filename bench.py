@@ -47,7 +47,7 @@ NCU_TRAFFIC: dict = {
     ("long_ctx", "plain"): {"bytes": 2974808000 + 7462144, "src": "87cc0cb0df187353"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
-    ("shared_prefix", "shared"): {"bytes": 853252864 + 7247616, "src": "863a21a50c94bb3c"},
+    ("shared_prefix", "shared"): {"bytes": 853222912 + 6847744, "src": "ec7652d90acf92b3"},
 }
 
 
