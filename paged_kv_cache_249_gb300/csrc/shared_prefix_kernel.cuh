@@ -358,14 +358,21 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             const bool has_next = j1 < total;
             const int j2 = fetch();
             const int f2 = field(j2);
-            int entn0 = -1, entn1 = -1, np1 = 0;
+            // (and its kv head, first block and length: its first stages go
+            // into the ring slots this item frees in its last NST blocks,
+            // since ring positions continue across items)
+            int entn0 = -1, entn1 = -1, np1 = 0, nx_g = 0, nx_b0 = 0, nx_nb = 0;
             if (has_next) {
                 const SpItem n1 = decode(j1, f1);
                 entn0 = bt_load(n1, 0);
                 entn1 = bt_load(n1, 1);
                 np1 = nparts_of(n1);
+                nx_g = n1.g;
+                nx_b0 = n1.b0;
+                nx_nb = n1.nb;
             }
             const bool two = it.R > 16;
+            unsigned issued = ctr + min(NST, it.nb);  // ring positions issued so far
             path.reset(lane);
             int cb = 0;
             bool ok = true;
@@ -395,27 +402,38 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                                                            a.scale_log2, lane);
                 }
                 __syncwarp();
-                if (i + NST < it.nb) issue(it.g, kk + NST, bt_get(i + NST), it.b0 + i + NST);
+                if (i + NST < it.nb) {
+                    issue(it.g, kk + NST, bt_get(i + NST), it.b0 + i + NST);
+                    issued = kk + NST + 1;
+                } else if (it.nb >= NST && i + NST - it.nb < nx_nb) {
+                    // next item's block j at position ctr + nb + j, in order
+                    // from j = 0 (an item shorter than NST leaves them all
+                    // to after the loop)
+                    const int j = i + NST - it.nb;  // < NST: within the first 32 entries
+                    issue(nx_g, kk + NST, __shfl_sync(FULL, entn0, j), nx_b0 + j);
+                    issued = kk + NST + 1;
+                }
             }
             if (!ok) {
                 if (lane == 0) raise_fault(a.dev_error, PKV_FAULT_TIMEOUT);
                 // drain what this warp still has in flight, again with a bound
-                for (int j = i; j < it.nb && j < i + NST; ++j) {
-                    const unsigned kk = ctr + j;
-                    mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
-                }
+                for (unsigned kk = ctr + i; kk < issued; ++kk) mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
                 break;
             }
-            ctr += it.nb;
             SpItem nx = it;
             if (has_next) {
-                // the next item's first stages and query rows, before this item's epilogue
+                // first stages the loop did not issue (all of them when this
+                // item had fewer than NST blocks), then the next query rows,
+                // before this item's epilogue
                 nx = decode(j1, f1);
 #pragma unroll 1
-                for (int j = 0; j < NST && j < nx.nb; ++j)
-                    issue(nx.g, ctr + j, __shfl_sync(FULL, entn0, j), nx.b0 + j);
+                for (unsigned p = issued; p < ctr + it.nb + min(NST, nx.nb); ++p) {
+                    const int j = (int)(p - ctr - it.nb);
+                    issue(nx.g, p, __shfl_sync(FULL, entn0, j), nx.b0 + j);
+                }
                 load_rows(nx);  // every lane is past its last ldmatrix of the buffer
             }
+            ctr += it.nb;
             // epilogue: rows gid and gid+8 of each tile, straight from registers
             const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
