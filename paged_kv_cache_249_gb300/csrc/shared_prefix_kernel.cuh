@@ -17,10 +17,10 @@
 // Work is a list written by the planning kernel and pulled, one item per
 // warp, from an atomic counter by a persistent grid: prefix items first (the
 // largest), then suffix items.  A warp runs its item alone, through its own
-// ring of TMA stages, so no warp ever waits for another: once it has consumed
-// its last block it stages the first blocks of its next item (whose entry,
+// ring of TMA stages, so no warp ever waits for another: the slots its last
+// blocks free already take the first blocks of its next item (whose entry,
 // block ids and partial counts it fetched while the current item streamed),
-// then writes its rows straight from registers.
+// and it writes its rows straight from registers while those land.
 #pragma once
 
 #include <math_constants.h>
