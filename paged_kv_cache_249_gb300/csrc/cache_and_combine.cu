@@ -132,7 +132,7 @@ pkv_status launch_bounded_wait_check(int32_t *dev_error, long long limit_ns, cud
 // which is exact: the partitions' exponentials share one max-free total.
 // Two kernels, chosen on the host by the number of partitions of the
 // longest allowed context.
-constexpr int kCombThreads = 128;
+constexpr int kCombThreads = 256;
 constexpr int kCombChunk = 1024;
 constexpr int kCombDirect = 16;  // up to this many partitions, the direct loop is faster
 
@@ -236,28 +236,44 @@ __global__ void __launch_bounds__(256)
     for (int j = 0; j < PER; ++j) comb_store(a, oi + j, den > 0.f ? num[j] / den : 0.f);
 }
 
-// Many partitions (a long context has hundreds): each (sequence, head) is
-// split over head_dim/32 CTAs of 32 columns, so the reads of the partials
-// have enough CTAs in flight.  A CTA computes the weights 2^(lse_p - M) once
-// into shared memory, kCombChunk parts at a time; four part groups of 32
-// threads then sum their columns over every fourth part, with eight
-// independent loads in flight per thread.
-constexpr int kCombCols = 32;
-constexpr int kCombGroups = kCombThreads / kCombCols;
+// Many partitions (a long context has hundreds): one CTA per (sequence,
+// head).  The CTA computes the weights 2^(lse_p - M) once into shared memory,
+// kCombChunk parts at a time; then warp w sums every kCombWarps-th part, each
+// lane owning D/32 adjacent columns (one 16-byte load per part for D = 128),
+// with kCombUnroll parts in flight, and the warps' sums meet in shared memory.
+constexpr int kCombWarps = kCombThreads / 32;
+constexpr int kCombUnroll = 8;
 
-__global__ void __launch_bounds__(kCombThreads)
-    lse_combine_many_kernel(const DecodeArgs a, int head_dim, int block_size) {
+template <int PER>
+__device__ __forceinline__ void comb_load(const float *p, float (&v)[PER]) {
+    if constexpr (PER == 8) {
+        const float4 x = *reinterpret_cast<const float4 *>(p);
+        const float4 y = *reinterpret_cast<const float4 *>(p + 4);
+        v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w, v[4] = y.x, v[5] = y.y, v[6] = y.z, v[7] = y.w;
+    } else if constexpr (PER == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(p);
+        v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    } else {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        v[0] = x.x, v[1] = x.y;
+    }
+}
+
+template <int PER>
+__global__ void __launch_bounds__(kCombThreads) lse_combine_many_kernel(const DecodeArgs a, int block_size) {
+    constexpr int D = PER * 32;
     __shared__ float w_s[kCombChunk];
-    __shared__ float red_m[kCombThreads / 32], red_d[kCombThreads / 32];
-    __shared__ float acc_s[kCombThreads];
+    __shared__ float red_m[kCombWarps], red_d[kCombWarps];
+    __shared__ __align__(16) float acc_s[kCombWarps][D];
     griddep_wait();  // the decode grid's partials are complete
-    const int slices = head_dim / kCombCols;
-    const CombRow r = comb_row(a, head_dim, block_size, blockIdx.x / slices);
+    const CombRow r = comb_row(a, D, block_size, blockIdx.x);
     if (r.nparts <= 1) return;  // the decode kernel wrote this row directly
     const float M = comb_max(r, red_m);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = (blockIdx.x % slices) * kCombCols + (tid % kCombCols), pg = tid / kCombCols;
-    float num = 0.f, den = 0.f;
+    float num[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) num[j] = 0.f;
+    float den = 0.f;
     for (int p0 = 0; p0 < r.nparts; p0 += kCombChunk) {
         const int n = r.nparts - p0 < kCombChunk ? r.nparts - p0 : kCombChunk;
         __syncthreads();  // the previous chunk's weights are consumed
@@ -267,29 +283,42 @@ __global__ void __launch_bounds__(kCombThreads)
             den += w;
         }
         __syncthreads();
-        const float *col = r.po + (size_t)p0 * head_dim + d;
-        int i = pg;
-        for (; i + 7 * kCombGroups < n; i += 8 * kCombGroups) {
-            float v[8];
+        const float *col = r.po + (size_t)p0 * D + lane * PER;
+        int i = warp;
+        for (; i + (kCombUnroll - 1) * kCombWarps < n; i += kCombUnroll * kCombWarps) {
+            float v[kCombUnroll][PER];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = col[(size_t)(i + u * kCombGroups) * head_dim];
+            for (int u = 0; u < kCombUnroll; ++u) comb_load<PER>(col + (size_t)(i + u * kCombWarps) * D, v[u]);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) num = fmaf(w_s[i + u * kCombGroups], v[u], num);
+            for (int u = 0; u < kCombUnroll; ++u) {
+                const float w = w_s[i + u * kCombWarps];
+#pragma unroll
+                for (int j = 0; j < PER; ++j) num[j] = fmaf(w, v[u][j], num[j]);
+            }
         }
-        for (; i < n; i += kCombGroups) num = fmaf(w_s[i], col[(size_t)i * head_dim], num);
+        for (; i < n; i += kCombWarps) {
+            float v[PER];
+            comb_load<PER>(col + (size_t)i * D, v);
+            const float w = w_s[i];
+#pragma unroll
+            for (int j = 0; j < PER; ++j) num[j] = fmaf(w, v[j], num[j]);
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
     if (lane == 0) red_d[warp] = den;
-    acc_s[tid] = num;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc_s[warp][lane * PER + j] = num[j];
     __syncthreads();
-    if (pg != 0) return;
     den = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCombThreads / 32; ++w) den += red_d[w];
+    for (int w = 0; w < kCombWarps; ++w) den += red_d[w];
+    for (int d = tid; d < D; d += kCombThreads) {
+        float x = 0.f;
 #pragma unroll
-    for (int q = 1; q < kCombGroups; ++q) num += acc_s[tid + q * kCombCols];
-    comb_store(a, (size_t)r.sh * head_dim + d, den > 0.f ? num / den : 0.f);
+        for (int w = 0; w < kCombWarps; ++w) x += acc_s[w][d];
+        comb_store(a, (size_t)r.sh * D + d, den > 0.f ? x / den : 0.f);
+    }
 }
 
 pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, int block_size,
@@ -307,9 +336,15 @@ pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, i
         return cuda_status(launch_dependent(lse_combine_kernel<4>, grid, dim3(256), 0, stream, a,
                                             block_size, (int)n));
     }
-    return cuda_status(launch_dependent(lse_combine_many_kernel,
-                                        dim3((unsigned)(n * (head_dim / kCombCols))),
-                                        dim3(kCombThreads), 0, stream, a, head_dim, block_size));
+    const dim3 grid((unsigned)n);
+    if (head_dim == 64)
+        return cuda_status(launch_dependent(lse_combine_many_kernel<2>, grid, dim3(kCombThreads), 0,
+                                            stream, a, block_size));
+    if (head_dim == 256)
+        return cuda_status(launch_dependent(lse_combine_many_kernel<8>, grid, dim3(kCombThreads), 0,
+                                            stream, a, block_size));
+    return cuda_status(launch_dependent(lse_combine_many_kernel<4>, grid, dim3(kCombThreads), 0, stream,
+                                        a, block_size));
 }
 
 }  // namespace pkv
