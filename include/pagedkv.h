@@ -277,8 +277,8 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * blocks are used), the offending group is then computed without sharing,
  * so the output is still exact.
  *
- * partition_tokens: 0 = automatic (parts of 512 tokens for the prefix and for
- * each sequence's own blocks), -1 = one part each, > 0 = parts of that many tokens (a
+ * partition_tokens: 0 = automatic (parts of 512 tokens for the prefix, of 256
+ * for each sequence's own blocks), -1 = one part each, > 0 = parts of that many tokens (a
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: BF16 or F16

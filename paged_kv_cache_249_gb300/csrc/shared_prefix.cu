@@ -13,8 +13,11 @@
 namespace pkv {
 namespace {
 
+// Automatic part sizes.  Prefix items carry up to 32 query rows and are
+// the long ones; suffix items (one sequence's own blocks, G rows) are cut
+// finer so the persistent grid ends on short items.
 constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic)
-constexpr int kAutoSuffixPartition = 512;   // tokens per suffix item (automatic)
+constexpr int kAutoSuffixPartition = 256;   // tokens per suffix item (automatic)
 constexpr int kPlanThreads = 1024;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

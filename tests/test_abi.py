@@ -195,7 +195,7 @@ def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib):
 def test_shared_prefix_workspace_bytes(lib):
     """Header, per-sequence counts and sharing records, the work list, and
     the partials: one slot per prefix part (512-token parts by default) and
-    per own part (512 tokens) of the longest sequence."""
+    per own part (256 tokens by default) of the longest sequence."""
     r = lambda x: -(-x // 256) * 256  # noqa: E731
 
     def expect(S, H, D, maxc, maxp, pt):
@@ -203,7 +203,7 @@ def test_shared_prefix_workspace_bytes(lib):
         if pt < 0:
             pp, ps = int(mp > 0), int(maxc > 0)
         else:
-            ptp = pts = pt if pt > 0 else 512
+            ptp, pts = (pt, pt) if pt > 0 else (512, 256)
             pp, ps = -(-mp // ptp), -(-maxc // pts)
         slots = max(pp + ps, 1)
         return (256 + r(S * 4) + r(S * 8) + r(S * slots * 32) + r(S * H * slots * 4) +
