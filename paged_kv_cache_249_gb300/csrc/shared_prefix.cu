@@ -119,8 +119,9 @@ struct PlanGroup {
 // description and counts the items of every size class; after a scan of the
 // class counts, the second pass reserves, per group, one range of entries
 // for its full-size items and one entry in the right class for each ragged
-// item, so no lane waits on more than two atomics in a row.  Context lengths
-// are read once, into shared memory.
+// item, so a group costs a few shared-memory atomics rather than one per
+// item.  Context lengths are read once, into shared memory (for up to
+// kPlanSmemSeqs sequences; a larger batch reads them where they are needed).
 __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(const SpPlan p) {
     constexpr unsigned FULL = 0xffffffffu;
     __shared__ int s_ctx[kPlanSmemSeqs];
