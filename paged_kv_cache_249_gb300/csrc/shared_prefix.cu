@@ -306,6 +306,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
 
 // ------------------------------------------------------------- combine
 
+// Drop one 128-byte line of dead scratch (a partial already consumed) from L2
+// without writing it back; its contents become undefined.  The shared-prefix
+// partials are stored without an L2 hint, so lines the combine has read
+// would otherwise be written back to DRAM while the next decode streams.
+__device__ __forceinline__ void l2_discard_line(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // One warp per (sequence, head): sequences with one part were written by the
 // decode kernel; zero parts (empty context) give a zero row; otherwise
 // out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M), M = max_p lse_p.
@@ -371,6 +379,10 @@ __global__ void __launch_bounds__(256) shared_prefix_combine_kernel(const SpArgs
 #pragma unroll
             for (int j = 0; j < PER; ++j) res[j] = den > 0.f ? num[j] / den : 0.f;
         }
+        // the partial rows are dead now: the lane at the start of each
+        // 128-byte line drops it from L2
+        if ((lane * PER) % 32 == 0)
+            for (int q = 0; q < np; ++q) l2_discard_line(po + (size_t)q * D);
     }
     const size_t oi = (size_t)wid * D + lane * PER;
 #pragma unroll
