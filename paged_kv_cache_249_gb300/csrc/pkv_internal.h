@@ -68,7 +68,7 @@ static_assert(sizeof(SpEntry) == 32, "work item is two 16-byte words");
 
 // Arguments of the persistent shared-prefix decode kernel.
 struct SpArgs {
-    const void *q;              // [S][H][D] bf16
+    const void *q;              // [S][H][D] pool dtype (bf16 or fp16)
     void *out;                  // [S][H][D] in out_dtype (fp32, bf16 or fp16)
     float *ws_o;                // [S][H][num_slots][D] partial outputs
     float *ws_lse;              // [S][H][num_slots] their log2-sum-exp
