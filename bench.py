@@ -47,7 +47,7 @@ NCU_TRAFFIC: dict = {
     ("long_ctx", "plain"): {"bytes": 2974808000 + 7462144, "src": "87cc0cb0df187353"},
     # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
     # include the plain kernel's header, so a change there re-dates it)
-    ("shared_prefix", "shared"): {"bytes": 853236480 + 7333632, "src": "6e04e78400c89d87"},
+    ("shared_prefix", "shared"): {"bytes": 853250816 + 7509248, "src": "16475fe6edf58568"},
 }
 
 

@@ -83,8 +83,8 @@ struct SpPlan {
     int ctx_cap;            // context lengths are clamped to [0, ctx_cap]
     int max_prefix_len;     // tokens (already capped by max_context_len)
     int block_size;         // tokens per pool block (a shared prefix is whole blocks)
-    int run_rows;           // tokens per staged run (min(block_size, 16)); the work list counts runs
-    int pbp, pbs;           // blocks per prefix / suffix item
+    int pbp, pbs;           // staged runs (16 tokens) per prefix / suffix item
+    int pbp_shift, pbs_shift;  // log2 of pbp / pbs when a power of two, else -1
     int cls_shift_p, cls_shift_s;  // size classes: (pbp - nb) >> cls_shift_p, likewise suffix
     int members_per_item;   // floor(32 / group)
     int num_heads, num_kv_heads, slots;  // recorded in the header for the run's check
@@ -93,6 +93,9 @@ struct SpPlan {
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+// x / d for x >= 0, with a shift when d is a power of two (sh = log2 d, else -1)
+__device__ __forceinline__ int div_by(int x, int d, int sh) { return sh >= 0 ? x >> sh : x / d; }
 
 // Items are listed largest first within each region (longest-processing-time
 // order): the persistent decode grid pulls them in list order, so its last
@@ -155,7 +158,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         return staged ? s_ctx[s] : clamp_ctx(__ldg(p.context_lens + s), p.ctx_cap);
     };
     const int ngr = flat ? p.num_seqs : p.num_groups;
-    const int BS = p.run_rows, mpi = p.members_per_item;
+    constexpr int BS = kMaxStageRows;  // the work list counts staged runs of 16 tokens
+    const int mpi = p.members_per_item;
 
     // members of group gi and the runs they share; a description that breaks
     // the rules shares nothing (and is reported)
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         if (plen == 0) return G;
         bool fits = true;
         for (int s = G.start + lane; s < G.end; s += 32) fits &= plen <= ctx_of(s);
-        const bool ok = __all_sync(FULL, fits) && plen > 0 && plen % p.block_size == 0 &&
+        const bool ok = __all_sync(FULL, fits) && plen > 0 && (plen & (p.block_size - 1)) == 0 &&
                         plen <= p.max_prefix_len;
         if (!ok) {
             if (lane == 0) raise_fault(p.dev_error, PKV_FAULT_PREFIX);
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         nb = (ctx + BS - 1) / BS;
         const int own = nb - pblk;
         if (own <= 0) return 0;
-        const int nq = (own + p.pbs - 1) / p.pbs;
+        const int nq = div_by(own + p.pbs - 1, p.pbs, p.pbs_shift);
         last = own - (nq - 1) * p.pbs;
         return nq;
     };
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     for (int gi = warp; gi < ngr; gi += nwarps) {
         const PlanGroup G = group_of(gi);
         if (G.pblk > 0 && lane == 0) {
-            const int pp = (G.pblk + p.pbp - 1) / p.pbp;
+            const int pp = div_by(G.pblk + p.pbp - 1, p.pbp, p.pbp_shift);
             const int sets = (G.end - G.start + mpi - 1) / mpi;
             if (pp > 1) atomicAdd(&s_cls[0][0], sets * (pp - 1));
             atomicAdd(&s_cls[0][cls_p(G.pblk - (pp - 1) * p.pbp)], sets);
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
 #pragma unroll 1
     for (int gi = warp; gi < ngr; gi += nwarps) {
         const PlanGroup G = group_of(gi);
-        const int pp = (G.pblk + p.pbp - 1) / p.pbp;
+        const int pp = div_by(G.pblk + p.pbp - 1, p.pbp, p.pbp_shift);
         if (pp > 0) {
             // item k of the group: member set k / pp, part k % pp; the full
             // parts of all sets take one range, the last parts another
@@ -435,6 +439,7 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
     if (pool->dtype == PKV_F32 || pool->head_dim > 128) return PKV_ERR_UNSUPPORTED;
     // blocks above kMaxStageRows tokens are staged (and listed) in runs
     c.U = c.BS < kMaxStageRows ? c.BS : kMaxStageRows;
+    if (c.U != kMaxStageRows) return PKV_ERR_UNSUPPORTED;  // blocks are whole 16-row runs
     c.unit_shift = 0;
     while ((c.U << c.unit_shift) < c.BS) ++c.unit_shift;
     if (((long long)max_blocks_per_seq << c.unit_shift) >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
@@ -477,7 +482,6 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
     p.ctx_cap = c.ctx_cap;
     p.max_prefix_len = c.maxp;
     p.block_size = c.BS;
-    p.run_rows = c.U;
     p.pbp = c.z.ptp > 0 ? c.z.ptp / c.U
                         : ((c.maxp + c.U - 1) / c.U > 0 ? (c.maxp + c.U - 1) / c.U : 1);
     p.pbs = c.z.pts > 0 ? c.z.pts / c.U : (c.cap_blocks > 0 ? c.cap_blocks : 1);
@@ -490,6 +494,13 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
     };
     p.cls_shift_p = cls_shift(p.pbp);
     p.cls_shift_s = cls_shift(p.pbs);
+    auto pow2_shift = [](int d) {
+        int sh = 0;
+        while ((1 << sh) < d) ++sh;
+        return (1 << sh) == d ? sh : -1;
+    };
+    p.pbp_shift = pow2_shift(p.pbp);
+    p.pbs_shift = pow2_shift(p.pbs);
     p.prefix_cap = num_seqs * c.z.pp;
     p.suffix_cap = num_seqs * c.z.ps;
     return cuda_status(launch_dependent(shared_prefix_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, p));
