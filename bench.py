@@ -7,7 +7,17 @@ sequence's new token (reshape_and_cache) followed by paged decode attention
 seeded synthetic workloads resident in HBM before timing starts.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --workload gqa_8b --dtype f16 --block-size 64 --only
   python bench.py --impl reference ...   # the float64 CPU oracle as the reference arm
+
+The default workload is long_ctx, the largest single-GPU batch (GQA 64/8
+heads, contexts of 32k-128k tokens split into 512-token partitions).  The
+same JSON line carries, under "other_workloads", the decode call of the
+gqa_8b, shared_prefix and mha_7b batches timed in the same process.  Shape
+flags (--dtype, --block-size, --head-dim, --num-heads, --num-kv-heads,
+--partition) rebuild the chosen workload's lengths and placement with other
+storage, block or head geometry; with any of them, or with --only, the other
+workloads are skipped.
 
 For N > 1 launch under torchrun; every rank runs its own batch (weak
 scaling, no collective on the data path) and rank 0 prints one JSON line.
@@ -32,21 +42,24 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-DEFAULT_WORKLOAD = "mha_7b"
+DEFAULT_WORKLOAD = "long_ctx"
+OTHER_WORKLOADS = ("gqa_8b", "shared_prefix", "mha_7b")
+# device time the decode-alone loop behind the roofline covers, at least
+ROOFLINE_SECONDS = 0.25
 METRIC = "paged decode attention effective KV-read GB/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes per decode launch from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by workload, valid only while the kernel
-# sources hash to `src`.  Filled in from the profiles summaries.
+# dram__bytes_write.sum of the decode kernel plus its combine), keyed by
+# workload and kernel family, valid only while the kernel sources hash to
+# `src`; a shape override (dtype, block or head size) has no record.
 NCU_TRAFFIC: dict = {
-    # profiles/paged_decode_kernel_mha_7b_gqa_8b_long_ctx.md
     ("mha_7b", "plain"): {"bytes": 1105054000 + 3578112, "src": "87cc0cb0df187353"},
     ("gqa_8b", "plain"): {"bytes": 2369795000 + 3299840, "src": "87cc0cb0df187353"},
     ("long_ctx", "plain"): {"bytes": 2974808000 + 7462144, "src": "87cc0cb0df187353"},
-    # profiles/shared_prefix_decode_kernel_shared_prefix.md (the shared-prefix kernel's sources
-    # include the plain kernel's header, so a change there re-dates it)
+    # the shared-prefix kernel's sources include the plain kernel's header,
+    # so a change there re-dates this record too
     ("shared_prefix", "shared"): {"bytes": 853250816 + 7509248, "src": "16475fe6edf58568"},
 }
 
@@ -82,11 +95,12 @@ def measured_peak_gbs() -> tuple[float, str]:
 
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples taken while the timed
-    region runs (read-only queries; no setting is changed)."""
+    regions run (read-only queries; no setting is changed)."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int = 0, period_ms: int = 20):
         self.samples: list[tuple[float, list[str]]] = []
@@ -110,28 +124,39 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
 
+    @staticmethod
+    def now() -> float:
+        return time.monotonic()
+
     def mark_start(self):
         self.window = (time.monotonic(), self.window[1])
 
     def mark_end(self):
         self.window = (self.window[0], time.monotonic())
-        time.sleep(0.05)
 
     def stop(self) -> dict:
+        """End sampling; the summary of the window marked by mark_start/mark_end."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+            return self.summary(0.0, 0.0)
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        t0, t1 = self.window
+        return self.summary(*self.window)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        """Median SM clock, the largest max clock and the active throttle
+        reasons of the samples taken between t0 and t1 (monotonic seconds)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         inside = [s for t, s in self.samples if t0 <= t <= t1]
         note = "timed region"
-        if not inside and self.samples:  # timed region shorter than the sampling period
+        if not inside and self.samples:  # region shorter than the sampling period
             nearest = min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))
             inside = [nearest[1]]
-            note = "nearest sample (timed region shorter than the sampling period)"
+            note = "nearest sample (region shorter than the sampling period)"
 
         def num(x):
             try:
@@ -141,12 +166,11 @@ class ClockSampler:
 
         sm = [num(s[1]) for s in inside if len(s) > 8 and num(s[1]) is not None]
         mx = [num(s[2]) for s in inside if len(s) > 8 and num(s[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in inside if len(s) > 8
+        reasons = sorted({self.REASONS[i] for s in inside if len(s) > 8
                           for i, v in enumerate(s[5:9]) if v.strip().lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(inside), "window": note}
+                "samples": len(inside), "seconds": round(t1 - t0, 3), "window": note}
 
 
 # ----------------------------------------------------------------- ranks --
@@ -193,6 +217,23 @@ def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> flo
 
 # ------------------------------------------------------------ workloads --
 
+def shape_overrides(args) -> dict:
+    """Keyword overrides of workload.make from the shape flags."""
+    ov = {}
+    for flag, key in (("dtype", "dtype"), ("block_size", "block_size"), ("head_dim", "head_dim"),
+                      ("num_heads", "num_heads"), ("num_kv_heads", "num_kv_heads"),
+                      ("partition", "partition_tokens")):
+        v = getattr(args, flag, None)
+        if v is not None:
+            ov[key] = v
+    return ov
+
+
+def make_workload(name: str, overrides: dict):
+    from paged_kv_cache_249_gb300 import workload as wl
+    return wl.make(name, **overrides)
+
+
 def algorithmic_bytes(w) -> dict:
     """Bytes the decode step must move at minimum (per rank, per step)."""
     e = w.elem_bytes
@@ -207,9 +248,12 @@ def algorithmic_bytes(w) -> dict:
             "decode_launch": kv_unique + q + out + table + w.num_seqs * 4}
 
 
-def workload_config(w, name: str, world: int) -> dict:
+def workload_config(w, name: str, world: int, overrides: dict | None = None) -> dict:
     from paged_kv_cache_249_gb300 import workload as wl
-    return {"workload": f"{name}: {wl.WORKLOADS[name]['desc']}", "num_seqs": w.num_seqs,
+    desc = f"{name}: {wl.WORKLOADS[name]['desc']}"
+    if overrides:
+        desc += " [shape flags: " + ", ".join(f"{k}={v}" for k, v in overrides.items()) + "]"
+    return {"workload": desc, "num_seqs": w.num_seqs,
             "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "kv_dtype": w.dtype, "out_dtype": "bf16",
             "accumulate": "f32", "mean_context": float(w.context_lens.mean()),
@@ -218,6 +262,55 @@ def workload_config(w, name: str, world: int) -> dict:
             "l2": f"inputs larger than L2 ({w.kv_bytes_unique() / 1e6:.0f} MB of unique KV per "
                   "step vs 129 MB L2); no flush",
             "parallelism": f"replicas x{world} (each rank its own batch)"}
+
+
+def shared_prefix_supported(w) -> bool:
+    """Shapes the shared-prefix decode takes (16-bit pools, heads up to 128
+    wide, blocks that are whole 16-row runs, groups up to 16)."""
+    return (w.dtype in ("bf16", "f16") and w.head_dim <= 128 and w.block_size % 16 == 0
+            and w.num_heads // w.num_kv_heads <= 16)
+
+
+def time_launches(fn, stream, min_seconds: float, warmup: int = 3,
+                  max_launches: int = 20000) -> dict:
+    """Launch fn back to back until the launches cover at least min_seconds
+    of device time, each bracketed by CUDA events on the launching stream.
+    Returns per-launch milliseconds (and the loop's monotonic window)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    probe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(3)]
+    for a_, b_ in probe:
+        a_.record(stream)
+        fn()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    per = max(1e-6, float(np.median([a_.elapsed_time(b_) for a_, b_ in probe])) / 1e3)
+    n = int(min(max_launches, max(20, np.ceil(min_seconds / per))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    t0 = time.monotonic()
+    for a_, b_ in ev:
+        a_.record(stream)
+        fn()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    ms = [a_.elapsed_time(b_) for a_, b_ in ev]
+    return {"ms": ms, "window": (t0, t1), "launches": n,
+            "device_seconds": float(np.sum(ms)) / 1e3}
+
+
+def launch_stats(ms: list, alg_bytes: int, peak: float) -> dict:
+    """Mean and median launch time and the roofline fraction of both."""
+    mean_s = float(np.mean(ms)) / 1e3
+    med_s = float(np.median(ms)) / 1e3
+    return {"us_mean": round(mean_s * 1e6, 2), "us_median": round(med_s * 1e6, 2),
+            "achieved_gbs": round(alg_bytes / mean_s / 1e9, 1),
+            "frac": round(alg_bytes / mean_s / 1e9 / peak, 4),
+            "frac_median": round(alg_bytes / med_s / 1e9 / peak, 4),
+            "launches": len(ms), "device_seconds": round(float(np.sum(ms)) / 1e3, 3)}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -267,29 +360,126 @@ def cpu_baseline(w, target_s: float = 12.0) -> dict:
 
 # ---------------------------------------------------------------- native --
 
+def _decode_path(args, w) -> bool:
+    """True when the step decodes through the shared-prefix entry point."""
+    if args.decode == "shared":
+        if not shared_prefix_supported(w):
+            raise SystemExit("bench.py: the shared-prefix decode does not take this shape "
+                             f"(dtype {w.dtype}, head_dim {w.head_dim}, block_size {w.block_size})")
+        return True
+    return args.decode == "auto" and w.group_size > 1 and shared_prefix_supported(w)
+
+
+def _setup_decode(dw, w, shared: bool, partition):
+    """(decode call, launches per step excluding the cache write, kernel family)."""
+    if shared:
+        dw.shared_prefix_setup(partition_tokens=partition or 0)
+        return dw.decode_shared_prefix, 3, "shared"  # plan, decode, combine
+    return dw.decode, 1 + (1 if dw.workspace is not None else 0), "plain"
+
+
+def _traffic(name: str, family: str, overrides: dict):
+    rec = NCU_TRAFFIC.get((name, family))
+    if overrides or not rec or rec.get("src") != kernel_source_hash(family):
+        return None
+    return rec["bytes"]
+
+
+def _cycles(us: float, clocks: dict):
+    """Launch time x median SM clock: SM cycles per launch (clock-normalised time)."""
+    mhz = clocks.get("sm_mhz") if clocks else None
+    return None if mhz is None else round(us * mhz)
+
+
+def _shared_prefix_extras(dw, w, ab, peak, stream, seconds: float) -> dict:
+    """On a shared-prefix batch: the plain decode of the same tables, and the
+    decode + combine of a run that reuses the step's plan (a model's later
+    layers).  Leaves the shared-prefix output in dw.out."""
+    ref_out = dw.out.clone()
+    pl = time_launches(dw.decode, stream, seconds)
+    plain_same = float((dw.out.float() - ref_out.float()).abs().max())
+    dw.shared_prefix_plan()
+    run = time_launches(dw.decode_shared_prefix_run, stream, seconds)
+    dw.decode_shared_prefix()
+    torch.cuda.synchronize()
+    pl_us = float(np.mean(pl["ms"])) * 1e3
+    return {"plain_decode_us": round(pl_us, 2),
+            "plain_decode_frac_logical_bytes": round(
+                (ab["kv_logical"] + ab["decode_launch"] - ab["kv_unique"]) / (pl_us * 1e-6) / 1e9
+                / peak, 4),
+            "max_abs_diff_plain_vs_shared": plain_same,
+            "per_layer_run": launch_stats(run["ms"], ab["decode_launch"], peak),
+            "per_layer_note": "decode + combine from one plan (a step's layers share its plan); "
+                              "the decode call above includes the plan"}
+
+
+def other_workload(name: str, args, peak: float, stream, clocks) -> dict:
+    """Step and decode-call timing of one more standard workload, in the same
+    process as the main line (decode loop of at least ROOFLINE_SECONDS)."""
+    from paged_kv_cache_249_gb300 import pagedkv
+    w = make_workload(name, {})
+    dw = pagedkv.DeviceWorkload(w, out_dtype=torch.bfloat16)
+    shared = _decode_path(argparse.Namespace(decode="auto"), w)
+    decode, n_dec, family = _setup_decode(dw, w, shared, None)
+    ab = algorithmic_bytes(w)
+
+    def step():
+        pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+        decode()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    step_s = t0.elapsed_time(t1) / 1e3 / args.steps
+    dec = time_launches(decode, stream, ROOFLINE_SECONDS)
+    st = launch_stats(dec["ms"], ab["decode_launch"], peak)
+    res = {"workload": workload_config(w, name, 1)["workload"],
+           "decode_path": "shared_prefix" if shared else "plain",
+           "step_us": round(step_s * 1e6, 2),
+           "effective_kv_gbs_step": round(ab["kv_logical"] / step_s / 1e9, 1),
+           "seqs_per_s": round(w.num_seqs / step_s, 1),
+           "seqs_per_s_decode_call": round(w.num_seqs / (st["us_mean"] * 1e-6), 1),
+           "decode_us_mean": st["us_mean"], "decode_us_median": st["us_median"],
+           "algorithmic_bytes_per_launch": ab["decode_launch"],
+           "bytes_basis": "unique (shared prefix once per group and kv head)" if shared
+           else "logical = unique",
+           "achieved_gbs": st["achieved_gbs"], "frac": st["frac"],
+           "frac_median": st["frac_median"], "peak": peak,
+           "launches": st["launches"], "device_seconds": st["device_seconds"],
+           "traffic": _traffic(name, family, {}),
+           "clocks": None, "sm_cycles_per_launch": None,  # filled in once sampling ends
+           "gpu_launches_per_step": 1 + n_dec, "_window": dec["window"]}
+    if shared:
+        res.update(_shared_prefix_extras(dw, w, ab, peak, stream, 0.1))
+    fault = pagedkv.get_device_error(dw.pool)
+    if fault:
+        raise SystemExit(f"bench.py: device fault bits {fault} on {name}")
+    del dw
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_native(args, world: int, rank: int) -> dict | None:
     from paged_kv_cache_249_gb300 import build as pkv_build
     from paged_kv_cache_249_gb300 import pagedkv
-    from paged_kv_cache_249_gb300 import workload as wl
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: the native arm needs a CUDA device")
     pkv_build.build()
     pagedkv.load()
-    w = wl.make(args.workload)
-    # the cache write must land where the oracle-side copy can still see
-    # the untouched pools for the CPU baseline
+    overrides = shape_overrides(args)
+    w = make_workload(args.workload, overrides)
+    peak, peak_kind = measured_peak_gbs()
     dw = pagedkv.DeviceWorkload(w, out_dtype=torch.bfloat16)
-    split = dw.workspace is not None
-    shared = args.decode == "shared" or (args.decode == "auto" and w.group_size > 1)
-    if shared:
-        dw.shared_prefix_setup()
-        decode = dw.decode_shared_prefix
-        launches_per_step = 1 + 3  # cache write, plan, decode, combine
-    else:
-        decode = dw.decode
-        launches_per_step = 2 + (1 if split else 0)
-    family = "shared" if shared else "plain"
+    shared = _decode_path(args, w)
+    decode, n_dec, family = _setup_decode(dw, w, shared, args.partition)
+    launches_per_step = 1 + n_dec
     stream = torch.cuda.current_stream()
     ab = algorithmic_bytes(w)
 
@@ -314,29 +504,23 @@ def run_native(args, world: int, rank: int) -> dict | None:
         step()
     t_end.record(stream)
     torch.cuda.synchronize()
-    # the decode call alone, for the roofline of its kernels
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for a_, b_ in ev_dec:
-        a_.record(stream)
-        decode()
-        b_.record(stream)
-    torch.cuda.synchronize()
+    # the decode call alone, for the roofline of its kernels: enough launches
+    # to cover ROOFLINE_SECONDS of device time
+    dec = time_launches(decode, stream, ROOFLINE_SECONDS, warmup=0)
     if clocks:
         clocks.mark_end()
     barrier(world)
     total_ms = t_start.elapsed_time(t_end)
-    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    dec_ms = dec["ms"]
     # the cache write alone (reported beside the decode, outside the timed step)
     ev_rc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(min(args.steps, 200))]
+             for _ in range(200)]
     for a_, b_ in ev_rc:
         a_.record(stream)
         pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
         b_.record(stream)
     torch.cuda.synchronize()
     rc_us = float(np.median([a_.elapsed_time(b_) for a_, b_ in ev_rc])) * 1e3
-    clock_info = clocks.stop() if clocks else None
     fault = pagedkv.get_device_error(dw.pool)
     if fault:
         raise SystemExit(f"bench.py: device fault bits {fault}")
@@ -368,42 +552,10 @@ def run_native(args, world: int, rank: int) -> dict | None:
     # ---- the plain decode kernel on the same batch (what prefix awareness buys)
     plain_cmp = None
     if shared and world == 1:
-        ref_out = dw.out.clone()
-        for _ in range(args.warmup):
-            dw.decode()
-        torch.cuda.synchronize()
-        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a_, b_ in pev:
-            a_.record(stream)
-            dw.decode()
-            b_.record(stream)
-        torch.cuda.synchronize()
-        pl_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in pev])) * 1e3
-        sp_us = float(np.mean(dec_ms)) * 1e3
-        # one plan serves every layer of a step: the decode and combine alone
-        dw.shared_prefix_plan()
-        for _ in range(args.warmup):
-            dw.decode_shared_prefix_run()
-        torch.cuda.synchronize()
-        rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a_, b_ in rev:
-            a_.record(stream)
-            dw.decode_shared_prefix_run()
-            b_.record(stream)
-        torch.cuda.synchronize()
-        run_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in rev])) * 1e3
-        plain_cmp = {"shared_prefix_decode_us": round(sp_us, 2), "plain_decode_us": round(pl_us, 2),
-                     "plain_over_shared": round(pl_us / sp_us, 4),
-                     "max_abs_diff": float((dw.out.float() - ref_out.float()).abs().max()),
-                     "per_layer_run_us": round(run_us, 2),
-                     "per_layer_run_frac": round(ab["decode_launch"] / (run_us * 1e-6) / 1e9 /
-                                                 measured_peak_gbs()[0], 4),
-                     "per_layer_note": "decode + combine from one plan (a step's layers share "
-                                       "its plan); the step above includes the plan"}
-        decode()  # leave the shared-prefix output in dw.out
-        torch.cuda.synchronize()
+        plain_cmp = _shared_prefix_extras(dw, w, ab, peak, stream, 0.1)
+        plain_cmp["shared_prefix_decode_us"] = round(float(np.mean(dec_ms)) * 1e3, 2)
+        plain_cmp["plain_over_shared"] = round(plain_cmp["plain_decode_us"] /
+                                               plain_cmp["shared_prefix_decode_us"], 4)
 
     # ---- the same decode over a contiguous cache (what paging costs)
     paging = None
@@ -416,17 +568,8 @@ def run_native(args, world: int, rank: int) -> dict | None:
                                                 dw.max_context_len, w.scale,
                                                 partition_tokens=dw.partition_tokens,
                                                 workspace=dw.workspace)
-        for _ in range(args.warmup):
-            contig_decode()
-        torch.cuda.synchronize()
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a_, b_ in cev:
-            a_.record(stream)
-            contig_decode()
-            b_.record(stream)
-        torch.cuda.synchronize()
-        c_us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in cev])) * 1e3
+        cl = time_launches(contig_decode, stream, 0.1)
+        c_us = float(np.mean(cl["ms"])) * 1e3
         p_us = float(np.mean(dec_ms)) * 1e3
         paging = {"paged_decode_us": round(p_us, 2), "contiguous_decode_us": round(c_us, 2),
                   "paged_over_contiguous": round(p_us / c_us, 4),
@@ -507,22 +650,35 @@ def run_native(args, world: int, rank: int) -> dict | None:
     e2e_value = whole_job_rate(ab["kv_logical"] * args.steps, world, e2e_s) / 1e9
     e2e_ok = all(torch.equal(o.view(torch.int16), dw.out.cpu().view(torch.int16)) for o in out_h) \
         if dw.out.dtype == torch.bfloat16 else None
+    fault = pagedkv.get_device_error(dw.pool)
+    if fault:
+        raise SystemExit(f"bench.py: device fault bits {fault}")
+    del dw, bufs
+    torch.cuda.empty_cache()
 
     if rank != 0:
         return None
-    peak, peak_kind = measured_peak_gbs()
-    dec_avg_s = float(np.mean(dec_ms)) / 1e3
-    achieved = ab["decode_launch"] / dec_avg_s / 1e9
-    traffic = None
-    rec = NCU_TRAFFIC.get((args.workload, family))
-    if rec and rec.get("src") == kernel_source_hash(family):
-        traffic = rec["bytes"]
+    st = launch_stats(dec_ms, ab["decode_launch"], peak)
+
+    # ---- the other standard workloads, timed in the same process
+    others = None
+    if world == 1 and not overrides and not args.only:
+        others = {name: other_workload(name, args, peak, stream, clocks)
+                  for name in OTHER_WORKLOADS if name != args.workload}
+    clock_info = clocks.stop() if clocks else None
+    roof_clocks = clocks.summary(*dec["window"]) if clocks else None
+    for res in (others or {}).values():
+        window = res.pop("_window")
+        if clocks:
+            res["clocks"] = clocks.summary(*window)
+            res["sm_cycles_per_launch"] = _cycles(res["decode_us_mean"], res["clocks"])
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1), PCG64)",
-        "config": workload_config(w, args.workload, world),
+        "config": workload_config(w, args.workload, world, overrides),
         "seqs_per_s": round(seqs_per_s, 1),
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
         # reported beside the KV bytes: the decode call's other traffic, the
@@ -533,16 +689,22 @@ def run_native(args, world: int, rank: int) -> dict | None:
         "side": {"q_bytes": ab["q"], "out_bytes": ab["out"], "block_table_bytes": ab["table"],
                  "context_len_bytes": w.num_seqs * 4, "new_kv_bytes": ab["new_kv"],
                  "reshape_and_cache_us": round(rc_us, 2),
-                 "seqs_per_s_decode_call": round(w.num_seqs / dec_avg_s, 1)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                 "seqs_per_s_decode_call": round(w.num_seqs / (st["us_mean"] * 1e-6), 1)},
+        "roofline": {"bound": "hbm", "achieved": st["achieved_gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": st["frac"],
+                     "traffic": _traffic(args.workload, family, overrides),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
                      "kernel": "shared_prefix_decode_kernel (+ plan and combine)" if shared
                      else "paged_decode_kernel (+ lse_combine when split)",
                      "algorithmic_bytes_per_launch": ab["decode_launch"],
-                     "decode_us_avg": round(dec_avg_s * 1e6, 2),
-                     "decode_us_median": round(float(np.median(dec_ms)) * 1e3, 2)},
+                     "bytes_basis": "unique (shared prefix once per group and kv head)"
+                     if shared else "logical = unique",
+                     "decode_us_avg": st["us_mean"], "decode_us_median": st["us_median"],
+                     "frac_median": st["frac_median"], "launches": st["launches"],
+                     "device_seconds": st["device_seconds"],
+                     "clocks": roof_clocks,
+                     "sm_cycles_per_launch": _cycles(st["us_mean"], roof_clocks)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3 / args.steps, 5),
                 "pipelining": "two input/output buffer sets; step k+1's host-to-device copies "
@@ -554,6 +716,9 @@ def run_native(args, world: int, rank: int) -> dict | None:
         "decode_path": "shared_prefix" if shared else "plain",
         "plain_decode_comparison": plain_cmp,
         "clocks": clock_info,
+        "clocks_note": "sampled every 20 ms from the first timed step to the end of the "
+                       "decode-alone loop behind roofline",
+        "other_workloads": others,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
@@ -570,7 +735,8 @@ def run_reference(args, world: int, rank: int) -> dict | None:
     import oracle
     from paged_kv_cache_249_gb300 import workload as wl
     oracle.build()
-    w = wl.make(args.workload)
+    overrides = shape_overrides(args)
+    w = make_workload(args.workload, overrides)
     threads = os.cpu_count() or 1
     step_budget = min(5.0, max(0.2, args.reference_seconds / max(1, args.steps + args.warmup)))
     sub, n = _oracle_sample(w, step_budget, threads)
@@ -588,7 +754,7 @@ def run_reference(args, world: int, rank: int) -> dict | None:
         "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), PCG64)", "impl": "reference",
-        "config": workload_config(w, args.workload, 1),
+        "config": workload_config(w, args.workload, 1, overrides),
         "seqs_per_s": round(n * args.steps / secs, 3),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
@@ -608,6 +774,17 @@ def main(argv=None):
     p.add_argument("--decode", choices=["auto", "plain", "shared"], default="auto",
                    help="decode entry point: auto = the shared-prefix kernel for batches "
                         "with shared-prefix groups, the plain kernel otherwise")
+    p.add_argument("--only", action="store_true",
+                   help="time the chosen workload alone (no other_workloads)")
+    p.add_argument("--dtype", choices=["bf16", "f16", "f32"], default=None,
+                   help="storage type of q, the pools and the new K/V (default: the workload's)")
+    p.add_argument("--block-size", type=int, choices=[16, 32, 64, 128, 256], default=None)
+    p.add_argument("--head-dim", type=int, choices=[64, 128, 256], default=None)
+    p.add_argument("--num-heads", type=int, default=None)
+    p.add_argument("--num-kv-heads", type=int, default=None)
+    p.add_argument("--partition", type=int, default=None,
+                   help="partition tokens: 0 = automatic, -1 = never split, N = N tokens "
+                        "(default: the workload's)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-contiguous", action="store_true",
                    help="skip the contiguous-cache comparison")

@@ -5,11 +5,11 @@
  * The operations follow the PagedAttention pages:
  *   - the KV cache is cut into fixed-size blocks that need not be contiguous
  *     in device memory (Qualiteg, "About PagedAttention for LLM serving",
- *     section "1-2 ... divides the KV cache into blocks", which suggests blocks
- *     of roughly 16 to 256 tokens);
+ *     "[Regarding Problem 1]", point 1-2; the same page puts a block at
+ *     roughly 16 to 256 tokens);
  *   - logical blocks of a sequence map onto physical blocks through a block
- *     table (same page, section "There are logical blocks and physical
- *     blocks, and the two are linked by a block table");
+ *     table (same page, the section on logical blocks, physical blocks and
+ *     the block table that links them);
  *   - the cache grows by one token per iteration (same page, "Characteristics
  *     of Autoregressive Models ..."), which pkv_reshape_and_cache writes;
  *   - attention is computed over the non-contiguous blocks without padding
@@ -205,12 +205,16 @@ pkv_status pkv_paged_attention_decode(const pkv_pool *pool, void *out, pkv_dtype
  * exits.  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
  * library routine.
  *  - The first call on a device looks the array's device address up
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
- *  - A call whose partials would need more than PKV_STATIC_SCRATCH_BYTES
- *    (pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim,
- *    max_context_len, partition_tokens)) returns PKV_ERR_WORKSPACE without
- *    launching anything.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *    life of the process; make that first call before any stream capture.
+ *    A cudaDeviceReset rebuilds the device's modules, so the kept address is
+ *    stale afterwards: do not use this entry point across a cudaDeviceReset.
+ *  - A call whose partials need more than PKV_STATIC_SCRATCH_BYTES returns
+ *    PKV_ERR_WORKSPACE without launching anything.  The need is the one the
+ *    decode computes for the partition it actually takes (with
+ *    partition_tokens = 0, the automatic choice of 512 to 2048 tokens), which
+ *    is at most pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim,
+ *    max_context_len, partition_tokens).
  *  - Every call on a device shares the one array and leaves its contents
  *    behind; nothing in it needs to start at zero (each partial is written
  *    before it is read).  Calls that overlap on the GPU (other streams, other
@@ -338,9 +342,10 @@ pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *src, const int32
 /*
  * Host-side block manager (host memory only, no CUDA call, not thread-safe).
  * It hands out physical blocks of a pool of num_blocks blocks as sequences
- * grow and takes them back when they finish (Qualiteg, "1-3 ... add or
- * remove blocks as needed"), keeps each sequence's logical-to-physical block
- * list ("There are logical blocks and physical blocks ..."), and lets forked
+ * grow and takes them back when they finish (Qualiteg, "[Regarding Problem
+ * 1]", point 1-3: blocks are taken and returned on demand instead of reserved
+ * up front), keeps each sequence's logical-to-physical block list (the same
+ * page's section on logical and physical blocks), and lets forked
  * sequences share blocks (prompt-prefix sharing) with reference counts:
  * appending to a shared, partly filled last block first moves the writer to
  * a fresh block and queues a (src, dst) copy for pkv_copy_blocks.

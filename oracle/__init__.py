@@ -8,8 +8,8 @@ pthreads); this module compiles it with gcc and marshals arguments.
 
 Definitions followed (see ``oracle.c`` for the full statement):
   * paged KV cache and block table -- Qualiteg, "About PagedAttention for LLM
-    serving", section "There are logical blocks and physical blocks, and the
-    two are linked by a block table";
+    serving", the section on logical blocks, physical blocks and the block
+    table that links them;
   * attention over the (non-contiguous) K and V -- vAttention, section 3.1
     "Requires re-writing the attention kernel" (standard softmax(q K^T scale) V,
     the formula the page names but does not print).

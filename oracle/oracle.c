@@ -9,9 +9,9 @@
  *
  * What it computes
  * ----------------
- * Paged KV cache (Qualiteg, "About PagedAttention for LLM serving", sections
- * "There are logical blocks and physical blocks, and the two are linked by a
- * block table" and "1-2 ... divides the KV cache into blocks"): the keys and
+ * Paged KV cache (Qualiteg, "About PagedAttention for LLM serving": the
+ * section on logical blocks, physical blocks and the block table, and point
+ * 1-2 under "[Regarding Problem 1]" on splitting the cache into blocks): the keys and
  * values of a sequence live in fixed-size blocks of a shared pool; logical
  * block i of sequence s is physical block block_tables[s][i].  Storage order
  * inside the pool (our choice, stated with the library): separate K and V

@@ -1,10 +1,11 @@
 // block_manager.cpp -- host-side manager of the physical block pool.
 //
 // The pages' memory manager: blocks are handed out as a sequence grows and
-// returned when it finishes ("as needed", Qualiteg, "1-3 ... PagedAttention
-// can add or remove blocks as needed"), each sequence's logical blocks map to
-// physical ones through its block table ("There are logical blocks and
-// physical blocks ..."), and requests that share a prompt prefix share its
+// returned when it finishes (on demand rather than reserved up front:
+// Qualiteg, "About PagedAttention for LLM serving", "[Regarding Problem 1]",
+// point 1-3), each sequence's logical blocks map to physical ones through its
+// block table (same page, the section on logical and physical blocks), and
+// requests that share a prompt prefix share its
 // KV blocks (the prefix-sharing use discussed on the Hacker News page).
 // Shared blocks are reference-counted; writing into a shared, partly filled
 // last block first moves the writer to a private copy (copy-on-write), which

@@ -12,7 +12,7 @@ namespace pkv {
 // The KV cache grows by one token per decode iteration (Qualiteg, "About
 // PagedAttention for LLM serving", "Characteristics of Autoregressive
 // Models..."); the new token's K and V rows go to the slot its block table
-// assigns ("There are logical blocks and physical blocks...").  One thread
+// assigns (same page, the section on logical and physical blocks).  One thread
 // moves one 16-byte chunk of one (token, kv head) row of K and of V, so a
 // warp writes whole 128-byte lines of the destination row.
 __global__ void __launch_bounds__(256)

@@ -3,8 +3,8 @@
 // One CTA computes the attention of the G query heads that share one KV head
 // (grouped-query attention, vAttention section 3.1) of one sequence over one
 // partition of its context.  The KV cache is read in place from the block
-// pool through the sequence's block table (Qualiteg, "There are logical
-// blocks and physical blocks, and the two are linked by a block table"), so
+// pool through the sequence's block table (Qualiteg, "About PagedAttention
+// for LLM serving", the section on logical and physical blocks), so
 // every (block, kv head) tile is read from HBM once per KV head, whatever G.
 //
 // Data movement: each warp owns NST shared-memory stages.  Lane 0 of the warp

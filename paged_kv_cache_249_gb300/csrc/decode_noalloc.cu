@@ -27,7 +27,9 @@ void *g_scratch_ptr[kMaxDevices];
 
 // Device address of g_decode_scratch on device `dev` (which must be current).
 // The symbol's name is only a host-side stand-in; the address must come from
-// cudaGetSymbolAddress, once per device.
+// cudaGetSymbolAddress, once per device.  The address is kept for the life of
+// the process: a cudaDeviceReset reloads the module and makes it stale, which
+// the header states as a limit of this entry point.
 pkv_status scratch_address(int dev, void **out) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_scratch_ptr[dev]) {
@@ -48,11 +50,9 @@ extern "C" pkv_status pkv_paged_attention_decode_static(
     const int32_t *context_lens, int max_context_len, float scale, int partition_tokens,
     int flags, void *stream) {
     if (!pool || pool->magic != pkv::kPoolMagic) return PKV_ERR_INVALID_ARG;
-    // Reject, before touching the device, any call whose partials would not
-    // fit in the fixed array.
-    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_heads, pool->head_dim,
-                                                   max_context_len, partition_tokens);
-    if (need > kScratchBytes) return PKV_ERR_WORKSPACE;
+    // A call whose partials do not fit in the fixed array is refused by the
+    // decode's own size check (PKV_ERR_WORKSPACE, before any launch), which
+    // sizes them for the partition it actually takes.
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;

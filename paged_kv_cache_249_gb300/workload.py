@@ -5,9 +5,9 @@ none of the attention arithmetic, so both the CUDA path and the float64
 oracle can take their inputs from it.
 
 Workload shapes follow the decode-step setting of the PagedAttention pages
-(Qualiteg, "About PagedAttention for LLM serving", sections "There are logical
-blocks and physical blocks, and the two are linked by a block table" and
-"1-2 ... divides the KV cache into blocks"): each running sequence owns a list
+(Qualiteg, "About PagedAttention for LLM serving": the section on logical
+blocks, physical blocks and the block table, and point 1-2 under "[Regarding
+Problem 1]" on splitting the KV cache into blocks): each running sequence owns a list
 of fixed-size logical blocks mapped through a per-sequence block table onto
 physical blocks of one shared pool, in no particular physical order.
 
@@ -267,7 +267,12 @@ def lengths(name: str) -> np.ndarray:
 
 
 def make(name: str, **overrides) -> Workload:
-    """Build a named workload with its fixed seeds."""
+    """Build a named workload with its fixed seeds.
+
+    ``overrides`` replace any keyword of ``build`` (dtype, head counts,
+    head_dim, block_size, partition_tokens, ...); the block table is then
+    sized from the workload's largest context for that block size.
+    """
     cid = WORKLOADS[name]["cid"]
     ctx = lengths(name)
     # lengths() consumed the first draws of the meta stream; placement uses a
@@ -276,22 +281,29 @@ def make(name: str, **overrides) -> Workload:
     data = DATA_SEED_BASE + cid
     if name == "tiny_f32":
         kw = dict(dtype="f32", num_heads=4, num_kv_heads=4, head_dim=64, block_size=16,
-                  pool_blocks=32, max_blocks_per_seq=4)
+                  pool_blocks=32)
+        max_tokens = 64
     elif name == "mha_7b":
-        kw = dict(dtype="bf16", num_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
-                  max_blocks_per_seq=2048 // 16)
+        kw = dict(dtype="bf16", num_heads=32, num_kv_heads=32, head_dim=128, block_size=16)
+        max_tokens = 2048
     elif name == "gqa_8b":
-        kw = dict(dtype="bf16", num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
-                  max_blocks_per_seq=8192 // 16)
+        kw = dict(dtype="bf16", num_heads=32, num_kv_heads=8, head_dim=128, block_size=16)
+        max_tokens = 8192
     elif name == "shared_prefix":
         kw = dict(dtype="bf16", num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
-                  max_blocks_per_seq=(4096 + 512) // 16, group_size=8, prefix_len=4096)
+                  group_size=8, prefix_len=4096)
+        max_tokens = 4096 + 512
     elif name == "long_ctx":
         kw = dict(dtype="bf16", num_heads=64, num_kv_heads=8, head_dim=128, block_size=16,
-                  max_blocks_per_seq=131072 // 16, partition_tokens=512)
+                  partition_tokens=512)
+        max_tokens = 131072
     else:
         raise KeyError(name)
     kw.update(overrides)
+    if "max_blocks_per_seq" not in overrides:
+        kw["max_blocks_per_seq"] = -(-max_tokens // kw["block_size"])
+    if name == "tiny_f32" and "pool_blocks" not in overrides and kw["block_size"] != 16:
+        kw.pop("pool_blocks")  # the 32-block pool is sized for 16-token blocks
     return build(name, context_lens=ctx, data_seed=data, meta_seed=meta, **kw)
 
 

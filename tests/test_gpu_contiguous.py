@@ -1,7 +1,8 @@
 """Paged = contiguous, on the GPU: the same tokens read through a block table
 from a shuffled pool, or from a conventional contiguous cache, give bitwise
 the same attention (the block table is an indirection only: Qualiteg,
-"There are logical blocks and physical blocks..."; vAttention section 3.1
+"About PagedAttention for LLM serving", the section on logical and physical
+blocks; vAttention section 3.1
 contrasts the two layouts)."""
 import pytest
 import torch

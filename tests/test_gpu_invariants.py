@@ -1,8 +1,9 @@
 """Invariants the PagedAttention pages fix, checked on the GPU, plus the
 degenerate and faulting inputs.
 
-The block table is an indirection only (Qualiteg, "There are logical blocks
-and physical blocks..."), so any physical placement of the same tokens must
+The block table is an indirection only (Qualiteg, "About PagedAttention for
+LLM serving", the section on logical and physical blocks), so any physical
+placement of the same tokens must
 give bitwise the same output: the kernel's arithmetic order depends only on
 logical positions.  Sequences that share prefix blocks (the prefix-sharing
 use discussed on the Hacker News page) must give bitwise the result of

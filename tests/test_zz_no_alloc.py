@@ -76,3 +76,29 @@ def test_static_scratch_rejects_partials_beyond_its_size():
     assert st == pagedkv.ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 0)  # nothing was launched
+
+
+@pytest.mark.gpu
+def test_static_scratch_long_context_automatic_partition():
+    """The full long-context batch (8 sequences of 32k-128k tokens, 64/8
+    heads) with the automatic partition: the decode takes 1024- or
+    2048-token partitions whose partials fit in the fixed array, although
+    the workspace bound for 512-token partitions does not."""
+    lib = pagedkv.load()
+    w = workload.make("long_ctx", partition_tokens=0)
+    assert pagedkv.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim,
+                                          w.max_context_len, 0) > pagedkv.STATIC_SCRATCH_BYTES
+    ref, _, _ = oracle_after_write(w)
+    dw = pagedkv.DeviceWorkload(w, partition_tokens=0)
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    dw.decode()
+    torch.cuda.synchronize()
+    expect = dw.out.clone()
+    assert_close(expect, ref, "bf16", "long_ctx workspace entry point")
+    for call in range(2):
+        got = torch.full_like(dw.out, float("nan"))
+        assert _call_static(lib, dw, got, 0) == pagedkv.OK
+        torch.cuda.synchronize()
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert torch.equal(got, expect), f"long_ctx call {call}: differs from the workspace call"
+        assert_close(got, ref, "bf16", f"long_ctx vs oracle, call {call}")
