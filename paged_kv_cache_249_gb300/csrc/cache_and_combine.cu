@@ -234,6 +234,9 @@ __global__ void __launch_bounds__(256)
     const size_t oi = (size_t)sh * D + lane * PER;
 #pragma unroll
     for (int j = 0; j < PER; ++j) comb_store(a, oi + j, den > 0.f ? num[j] / den : 0.f);
+    // (the consumed partials are left in L2 here: dropping them, as the
+    // many-partition combine does, measured 0.45 % slower on 128 sequences
+    // of 512-8192 tokens in 1024-token parts)
 }
 
 // Many partitions (a long context has hundreds): one CTA per (sequence,
@@ -319,6 +322,10 @@ __global__ void __launch_bounds__(kCombThreads) lse_combine_many_kernel(const De
         for (int w = 0; w < kCombWarps; ++w) x += acc_s[w][d];
         comb_store(a, (size_t)r.sh * D + d, den > 0.f ? x / den : 0.f);
     }
+    // every warp has used its loads (the barrier above): the row's partial
+    // lines are dead, and would otherwise be written back from L2 during the
+    // next decode (48 MB per call on a 128k-token batch in 512-token parts)
+    for (int q = tid; q < r.nparts * (D / 32); q += kCombThreads) l2_discard_line(r.po + (size_t)q * 32);
 }
 
 pkv_status launch_lse_combine(const DecodeArgs &a, int num_seqs, int head_dim, int block_size,

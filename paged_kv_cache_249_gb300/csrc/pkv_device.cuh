@@ -132,6 +132,14 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     return p;
 }
 
+// Drop one 128-byte line of dead scratch (a partial already consumed) from L2
+// without writing it back; its contents become undefined.  Split partials
+// are written and read back through L2; a consumed line that stays dirty
+// there is written back to DRAM while the next decode streams.
+__device__ __forceinline__ void l2_discard_line(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Stores with an L2 cache policy.
 __device__ __forceinline__ void st_f32_hint(float *ptr, float v, uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy)

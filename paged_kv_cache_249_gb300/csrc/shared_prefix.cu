@@ -310,13 +310,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
 
 // ------------------------------------------------------------- combine
 
-// Drop one 128-byte line of dead scratch (a partial already consumed) from L2
-// without writing it back; its contents become undefined.  The shared-prefix
-// partials are stored without an L2 hint, so lines the combine has read
-// would otherwise be written back to DRAM while the next decode streams.
-__device__ __forceinline__ void l2_discard_line(const void *p) {
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
+// The shared-prefix partials are stored without an L2 hint; once consumed,
+// l2_discard_line drops them so they are not written back to DRAM while the
+// next decode streams.
 
 // One warp per (sequence, head): sequences with one part were written by the
 // decode kernel; zero parts (empty context) give a zero row; otherwise
