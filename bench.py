@@ -265,9 +265,9 @@ def workload_config(w, name: str, world: int, overrides: dict | None = None) -> 
 
 
 def shared_prefix_supported(w) -> bool:
-    """Shapes the shared-prefix decode takes (16-bit pools, heads up to 128
-    wide, blocks that are whole 16-row runs, groups up to 16)."""
-    return (w.dtype in ("bf16", "f16") and w.head_dim <= 128 and w.block_size % 16 == 0
+    """Shapes the shared-prefix decode takes (16-bit pools, blocks that are
+    whole 16-row runs, groups up to 16)."""
+    return (w.dtype in ("bf16", "f16") and w.block_size % 16 == 0
             and w.num_heads // w.num_kv_heads <= 16)
 
 

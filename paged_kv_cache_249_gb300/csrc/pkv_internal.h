@@ -16,6 +16,9 @@ constexpr int kMaxPartitionTokens = 8192;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxStageRows = 16;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
+// Query rows of a shared-prefix work item for a head size: two 16-row tiles
+// up to 128 columns, one tile of a 256-wide head (the same accumulator registers).
+constexpr int sp_rows_for(int head_dim) { return head_dim > 128 ? 16 : kSpRowsMax; }
 
 // Arguments of one decode launch; every pointer is a device pointer.
 struct DecodeArgs {
@@ -124,6 +127,8 @@ pkv_status launch_shared_prefix_d64(const SpLaunch &L);       // bf16 pools
 pkv_status launch_shared_prefix_d128(const SpLaunch &L);      // bf16 pools
 pkv_status launch_shared_prefix_f16_d64(const SpLaunch &L);
 pkv_status launch_shared_prefix_f16_d128(const SpLaunch &L);
+pkv_status launch_shared_prefix_d256(const SpLaunch &L);      // bf16 pools
+pkv_status launch_shared_prefix_f16_d256(const SpLaunch &L);
 
 pkv_status launch_decode_f32_d64(const DecodeLaunch &L);
 pkv_status launch_decode_f32_d128(const DecodeLaunch &L);

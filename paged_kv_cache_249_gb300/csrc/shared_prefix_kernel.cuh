@@ -9,7 +9,8 @@
 // then needs to come from HBM once for the whole group, not once per
 // sequence: a "prefix item" stages a block once and multiplies it against
 // the query rows of every member (members x GQA group <= 32 rows, two 16-row
-// mma.sync tiles), while "suffix items" walk each sequence's own blocks.
+// mma.sync tiles; 16 rows, one tile, for a 256-wide head), while "suffix
+// items" walk each sequence's own blocks.
 // Every item leaves a normalised partial output and its log2-sum-exp per
 // query row (or the final row when it is the sequence's only part); the
 // combine pass merges the parts, which is exact for softmax.
@@ -30,14 +31,20 @@
 namespace pkv {
 
 constexpr int kSpWarps = 4;
+// query rows and 16-row accumulator tiles of one item
+template <int D>
+constexpr int kSpRows = sp_rows_for(D);
+template <int D>
+constexpr int kSpTiles = kSpRows<D> / 16;
 // Shared memory per CTA: two CTAs (8 warps) per SM, which is what the
-// register budget of the two-tile accumulators allows.
+// register budget of the two-tile accumulators allows (a 256-wide head's
+// 16 KiB stages fit one CTA per SM).
 constexpr int kSpSmemTarget = 112 * 1024;
 
 template <int D, int BS>
 struct SpSmem {
     using Gm = Geom<__nv_bfloat16, D, BS>;  // sizes only: the same for fp16
-    static constexpr int kQ = kSpRowsMax * D * 2;  // a warp's query rows (16-bit, swizzled slabs)
+    static constexpr int kQ = kSpRows<D> * D * 2;  // a warp's query rows (16-bit, swizzled slabs)
     static constexpr int kMisc = 256;
     static constexpr int kFixed = kSpWarps * kQ + kMisc + 1024;
     static constexpr int kStagesFit = (kSpSmemTarget - kFixed) / (kSpWarps * Gm::kStageBytes);
@@ -77,15 +84,16 @@ template <typename T, int D, int BS>
 struct SpMma {
     using MM = Mma16<T>;
     static constexpr int ND = D / 8;  // n-tiles of O
-    float o[2][ND][4];
-    float m[2][2], l[2][2];  // [tile][row gid / gid+8]; l is lane-partial
+    static constexpr int NT = kSpTiles<D>;
+    float o[NT][ND][4];
+    float m[NT][2], l[NT][2];  // [tile][row gid / gid+8]; l is lane-partial
     int gid, tig;
 
     __device__ __forceinline__ void reset(int lane) {
         gid = lane >> 2;
         tig = lane & 3;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NT; ++t) {
             m[t][0] = m[t][1] = -CUDART_INF_F;
             l[t][0] = l[t][1] = 0.f;
 #pragma unroll
@@ -333,7 +341,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 src = qg + ((size_t)sq * a.num_heads + h) * D + c * 8;
                 bytes = 16;
             }
-            cp_async16(qaddr + swz_offset<kSpRowsMax>(r, c), src, bytes);
+            cp_async16(qaddr + swz_offset<kSpRows<D>>(r, c), src, bytes);
         }
         cp_async_commit();
     };
@@ -394,12 +402,17 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 if (pb >= 0 && pb < a.num_blocks) {
                     const int nvalid = min(BS, it.tok_end - (it.b0 + i) * BS);
                     const uint32_t kaddr = smem_u32(wstage + (kk % NST) * Gm::kStageBytes);
-                    if (two)
-                        path.template block<2, kSpRowsMax>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
+                    if constexpr (kSpTiles<D> == 2) {
+                        if (two)
+                            path.template block<2, kSpRows<D>>(kaddr, kaddr + Gm::kTileBytes, qaddr,
+                                                               nvalid, a.scale_log2, lane);
+                        else
+                            path.template block<1, kSpRows<D>>(kaddr, kaddr + Gm::kTileBytes, qaddr,
+                                                               nvalid, a.scale_log2, lane);
+                    } else {
+                        path.template block<1, kSpRows<D>>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
                                                            a.scale_log2, lane);
-                    else
-                        path.template block<1, kSpRowsMax>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
-                                                           a.scale_log2, lane);
+                    }
                 }
                 __syncwarp();
                 if (i + NST < it.nb) {
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             // epilogue: rows gid and gid+8 of each tile, straight from registers
             const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
+            for (int t = 0; t < kSpTiles<D>; ++t) {
                 if (t == 1 && !two) break;
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {

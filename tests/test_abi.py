@@ -187,7 +187,8 @@ def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib):
     assert _sp_decode(lib, pool, num_kv_heads=4) == E                # != pool heads
     assert _sp_decode(lib, pool, scale=float("inf")) == E
     assert _sp_decode(lib, _fake_pool(dtype=pagedkv.F32)) == U       # bf16 or fp16 pools only
-    assert _sp_decode(lib, _fake_pool(head_dim=256)) == U            # head size 64 or 128
+    # a 256-wide head passes the shape checks (here it stops at the missing workspace)
+    assert _sp_decode(lib, _fake_pool(head_dim=256), ws_bytes=0) == pagedkv.ERR_WORKSPACE
     assert _sp_decode(lib, pool, num_heads=34) == U                  # group 17 > 16
     assert _sp_decode(lib, pool, num_seqs=0) == pagedkv.OK           # nothing to do
 

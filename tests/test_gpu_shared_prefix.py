@@ -7,8 +7,8 @@ the attention result is the same as for private copies, which the oracle
 computes by gathering each sequence's blocks through its own table.  The
 cases cover ragged groups, every GQA group size the kernel packs (1 to 16
 query heads per KV head, with members split across 32-row work items),
-empty suffixes, partial last blocks, both head sizes and block sizes, both
-output types, and group descriptions that break the rules (reported in the
+empty suffixes, partial last blocks, head sizes 64, 128 and 256, block sizes
+16 to 256, both output types, and group descriptions that break the rules (reported in the
 error word; the output must still be exact).
 """
 import numpy as np
@@ -69,6 +69,10 @@ CASES = {
     "d64_bs16_mha": (_prefix_ctx(48, [1, 2, 3]), [(3, 48)], 4, 4, 64, 16),
     "big_group": (_prefix_ctx(1024, list(range(1, 40 * 7, 7))), [(40, 1024)], 8, 8, 128, 16),
     "varied_groups": (*_varied_groups(), 8, 2, 128, 16),
+    # 256-wide heads: one 16-row tile per item (16 / G members)
+    "d256_g4": (_prefix_ctx(256, [0, 1, 17, 100, 300]), [(5, 256)], 16, 4, 256, 16),
+    "d256_g8_bs64": (_prefix_ctx(128, [3, 64, 65]), [(3, 128)], 16, 2, 256, 64),
+    "d256_g1_mha": (_prefix_ctx(96, list(range(1, 120, 7))), [(17, 96)], 4, 4, 256, 16),
 }
 
 
@@ -85,7 +89,7 @@ def test_shared_prefix_matches_oracle(case, partition):
     assert_close(dw.out, ref, "bf16", f"{case} partition {partition}")
 
 
-@pytest.mark.parametrize("case", ["g4_eight_members", "g4_ragged_groups", "d64_bs32"])
+@pytest.mark.parametrize("case", ["g4_eight_members", "g4_ragged_groups", "d64_bs32", "d256_g8_bs64"])
 def test_shared_prefix_bf16_output(case):
     ctx, groups, H, Hkv, D, BS = CASES[case]
     w = _w(case, ctx, groups, H, Hkv, D, BS, seed=3)
@@ -303,7 +307,7 @@ def test_shared_prefix_large_block_tables_that_differ_are_reported():
 
 # ------------------------------------------------------------- fp16 pools
 
-@pytest.mark.parametrize("case", ["g4_ragged_groups", "g8_two_items", "d64_bs32"])
+@pytest.mark.parametrize("case", ["g4_ragged_groups", "g8_two_items", "d64_bs32", "d256_g4"])
 def test_shared_prefix_f16(case):
     ctx, groups, H, Hkv, D, BS = CASES[case]
     w = workload.build(case, dtype="f16", context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
@@ -345,6 +349,32 @@ def test_shared_prefix_random_sweep():
         dw = _run(w, pt)
         assert pagedkv.get_device_error(dw.pool) == 0, trial
         assert_close(dw.out, ref, dtype, f"trial {trial}: BS{BS} D{D} G{G} groups {groups} pt {pt}")
+
+
+def test_shared_prefix_random_sweep_d256():
+    """The same sweep for 256-wide heads (items of 16 rows: 16 / G members)."""
+    rng = np.random.default_rng(2256)
+    for trial in range(6):
+        BS = int(rng.choice([16, 32, 64]))
+        Hkv = int(rng.integers(1, 3))
+        G = int(rng.choice([1, 2, 4, 8, 16]))
+        dtype = ["bf16", "f16"][trial % 2]
+        groups, ctx = [], []
+        for _ in range(int(rng.integers(1, 4))):
+            members = int(rng.integers(1, 10))
+            prefix = BS * int(rng.integers(0, 5)) if members > 1 else 0
+            groups.append((members, prefix))
+            own = [int(rng.integers(1, 250)) for _ in range(members)]
+            own[0] = int(rng.integers(0, 250))
+            ctx += [prefix + o for o in own]
+        w = workload.build(f"sweep256_{trial}", dtype=dtype, context_lens=ctx, num_heads=Hkv * G,
+                           num_kv_heads=Hkv, head_dim=256, block_size=BS, data_seed=9300 + trial,
+                           meta_seed=9400 + trial, groups=groups)
+        ref, _, _ = oracle_after_write(w)
+        pt = int(rng.choice([0, -1, BS, 4 * BS]))
+        dw = _run(w, pt)
+        assert pagedkv.get_device_error(dw.pool) == 0, trial
+        assert_close(dw.out, ref, dtype, f"trial {trial}: BS{BS} G{G} groups {groups} pt {pt}")
 
 
 def test_more_sequences_than_the_plan_stages():
