@@ -107,8 +107,8 @@ size_t pkv_pool_bytes(int num_blocks, int block_size, int num_kv_heads, int head
  * non-zero clears both pools and the error word on `stream`.
  * Supported: block_size in {16, 32, 64, 128, 256} (the page's range of
  * roughly 16 to 256 tokens; the kernels stage every block in runs of 16
- * rows); head_dim in {64, 128, 256} (256: the decode takes BF16 or F16
- * pools; the shared-prefix decode takes 64 or 128); dtype F32, BF16 or F16;
+ * rows); head_dim in {64, 128, 256} (256: BF16 or F16 pools); dtype F32,
+ * BF16 or F16 (the shared-prefix decode takes BF16 or F16 pools);
  * num_blocks*num_kv_heads*block_size < 2^31.
  */
 pkv_status pkv_block_pool_init(pkv_pool *pool, int num_blocks, int block_size, int num_kv_heads,
@@ -286,7 +286,9 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: BF16 or F16
- * pools, num_heads / num_kv_heads in 1..16, out_dtype F32, BF16 or F16.
+ * pools (head_dim 64, 128 or 256; a 256-wide head's work items carry 16
+ * query rows instead of 32), num_heads / num_kv_heads in 1..16, out_dtype
+ * F32, BF16 or F16.
  */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_context_len, int max_prefix_len,
