@@ -8,7 +8,6 @@ block tables with ordinary device kernels immediately before each decode,
 with no synchronisation in between, and check the result against the
 oracle on the changed inputs.
 """
-import numpy as np
 import pytest
 import torch
 
