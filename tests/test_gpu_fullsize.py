@@ -1,7 +1,8 @@
 """Full-size decode workloads, in the launch configuration the benchmark
 times (bf16 output, automatic or workload-given partitioning, automatic
 compute path), compared with the float64 oracle on every sequence and every
-element.
+element; the shared-prefix batch also with 256-wide heads (its items then
+carry 16 query rows).
 
 The oracle computes each sequence's result through its own block table
 (Qualiteg, "About PagedAttention for LLM serving", the section on logical
@@ -18,7 +19,17 @@ from tests.gpu_helpers import assert_close, oracle_after_write
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["mha_7b", "gqa_8b", "shared_prefix", "long_ctx"]
+FULL = ["mha_7b", "gqa_8b", "shared_prefix", "long_ctx", "shared_prefix/head_dim=256"]
+
+
+def _make(param):
+    """A workload by name, with an optional shape override after a slash."""
+    name, _, over = param.partition("/")
+    kw = {}
+    if over:
+        k, v = over.split("=")
+        kw[k] = int(v)
+    return workload.make(name, **kw)
 
 
 def _bits(t: torch.Tensor) -> torch.Tensor:
@@ -30,7 +41,7 @@ def _bits(t: torch.Tensor) -> torch.Tensor:
 def full(request):
     """A full-size workload with the oracle's pools after the cache write and
     its float64 output for the whole batch."""
-    w = workload.make(request.param)
+    w = _make(request.param)
     ref, kp, vp = oracle_after_write(w)
     yield request.param, w, ref, kp, vp
 
