@@ -2,7 +2,8 @@
 times (bf16 output, automatic or workload-given partitioning, automatic
 compute path), compared with the float64 oracle on every sequence and every
 element; the shared-prefix batch also with 256-wide heads (its items then
-carry 16 query rows).
+carry 16 query rows), the GQA batch with fp16 pools and the MHA batch in
+64-token blocks.
 
 The oracle computes each sequence's result through its own block table
 (Qualiteg, "About PagedAttention for LLM serving", the section on logical
@@ -19,7 +20,8 @@ from tests.gpu_helpers import assert_close, oracle_after_write
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["mha_7b", "gqa_8b", "shared_prefix", "long_ctx", "shared_prefix/head_dim=256"]
+FULL = ["mha_7b", "gqa_8b", "shared_prefix", "long_ctx", "shared_prefix/head_dim=256",
+        "gqa_8b/dtype=f16", "mha_7b/block_size=64"]
 
 
 def _make(param):
@@ -28,8 +30,12 @@ def _make(param):
     kw = {}
     if over:
         k, v = over.split("=")
-        kw[k] = int(v)
+        kw[k] = v if k == "dtype" else int(v)
     return workload.make(name, **kw)
+
+
+def _tol(w):
+    return "f16" if w.dtype == "f16" else "bf16"
 
 
 def _bits(t: torch.Tensor) -> torch.Tensor:
@@ -62,13 +68,13 @@ def test_fullsize_plain_decode_whole_batch(full):
     dw.step()
     torch.cuda.synchronize()
     assert pagedkv.get_device_error(dw.pool) == 0
-    assert_close(dw.out, ref, "bf16", f"{name} bf16 output, all {w.num_seqs} sequences")
+    assert_close(dw.out, ref, _tol(w), f"{name} bf16 output, all {w.num_seqs} sequences")
     # the same launch with fp32 output, graded at the 2e-3 tolerance alone
     dw32 = pagedkv.DeviceWorkload(w, out_dtype=torch.float32)
     dw32.step()
     torch.cuda.synchronize()
     assert pagedkv.get_device_error(dw32.pool) == 0
-    assert_close(dw32.out, ref, "bf16", f"{name} fp32 output, all {w.num_seqs} sequences")
+    assert_close(dw32.out, ref, _tol(w), f"{name} fp32 output, all {w.num_seqs} sequences")
     # the bf16 output is the fp32 output rounded once
     assert torch.equal(_bits(dw32.out.to(torch.bfloat16)), _bits(dw.out))
 
@@ -85,7 +91,7 @@ def test_fullsize_shared_prefix_decode_whole_batch(full):
         dw.decode_shared_prefix()
         torch.cuda.synchronize()
         assert pagedkv.get_device_error(dw.pool) == 0
-        assert_close(dw.out, ref, "bf16",
+        assert_close(dw.out, ref, _tol(w),
                      f"{name} shared-prefix decode, {out_dtype}, all {w.num_seqs} sequences")
         # a second run from the same plan (a model's next layer) gives the same bits
         first = dw.out.clone()
