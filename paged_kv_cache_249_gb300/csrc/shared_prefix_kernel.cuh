@@ -86,15 +86,19 @@ struct SpMma {
     static constexpr int ND = D / 8;  // n-tiles of O
     static constexpr int NT = kSpTiles<D>;
     float o[NT][ND][4];
-    float m[NT][2], l[NT][2];  // [tile][row gid / gid+8]; l is lane-partial
+    // [tile][row gid / gid+8]: m is the row's reference (log2 units), l its
+    // lane-partial sum of weights relative to m
+    float m[NT][2], l[NT][2];
     int gid, tig;
+    bool fresh;  // no block seen yet: the first one sets every row's reference
 
     __device__ __forceinline__ void reset(int lane) {
         gid = lane >> 2;
         tig = lane & 3;
+        fresh = true;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            m[t][0] = m[t][1] = -CUDART_INF_F;
+            m[t][0] = m[t][1] = 0.f;
             l[t][0] = l[t][1] = 0.f;
 #pragma unroll
             for (int n = 0; n < ND; ++n) o[t][n][0] = o[t][n][1] = o[t][n][2] = o[t][n][3] = 0.f;
@@ -106,6 +110,17 @@ struct SpMma {
     template <int MT, int QR>
     __device__ __forceinline__ void sub_block(uint32_t kaddr, uint32_t vaddr, uint32_t qaddr,
                                               int r0, int nvalid, float scale_log2, int lane) {
+        const bool partial = nvalid < 16;  // the item's last run only (warp-uniform)
+        if (partial) {
+            // V rows past the context may hold stale bits (even NaN, and 0 * NaN
+            // is NaN): zero them in the stage before P V reads it.  The fence
+            // orders these writes before the TMA refill of the slot.
+            constexpr int CH = D * 2 / 16;
+            for (int q = lane; q < (16 - nvalid) * CH; q += 32)
+                sts_zero16(vaddr + swz_offset<BS>(r0 + nvalid + q / CH, q % CH));
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
         float s[MT][2][4];
 #pragma unroll
         for (int t = 0; t < MT; ++t)
@@ -137,50 +152,95 @@ struct SpMma {
                     for (int t = 0; t < MT; ++t)
                         MM::mma(s[t][nt], qa[t][h], kb[nt][2 * h], kb[nt][2 * h + 1]);
         }
-        // online softmax per row (log2 domain)
-        uint32_t ph[MT][4], pl[MT][4];
+        // Online softmax per row (log2 domain) against a lazy reference: a
+        // row's reference m moves, and its sum and accumulators are rescaled,
+        // only when one of its scores passes m by more than kLazyLog2.  Until
+        // then the weights stay at most 2^kLazyLog2, which the 16-bit high part
+        // and remainder of P carry with the same relative precision as weights
+        // below 1, and the final division by the row's sum is unchanged
+        // (softmax does not depend on the reference subtracted).  Most blocks
+        // then skip the row-max shuffles and the multiply of every accumulator;
+        // the score scale and the subtraction of m are one fused multiply-add.
+        constexpr float kLazyLog2 = 8.f;
+        if (partial) {
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (nt * 8 + 2 * tig + e >= nvalid)
+                            s[t][nt][e] = s[t][nt][2 + e] = -CUDART_INF_F;
+        }
+        bool grow = fresh;
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool ok = nt * 8 + 2 * tig + e < nvalid;
-                    s[t][nt][e] = ok ? s[t][nt][e] * scale_log2 : -CUDART_INF_F;
-                    s[t][nt][2 + e] = ok ? s[t][nt][2 + e] * scale_log2 : -CUDART_INF_F;
-                    mx0 = fmaxf(mx0, s[t][nt][e]);
-                    mx1 = fmaxf(mx1, s[t][nt][2 + e]);
+                    s[t][nt][e] = fmaf(s[t][nt][e], scale_log2, -m[t][0]);
+                    s[t][nt][2 + e] = fmaf(s[t][nt][2 + e], scale_log2, -m[t][1]);
+                    grow |= s[t][nt][e] > kLazyLog2;
+                    grow |= s[t][nt][2 + e] > kLazyLog2;
                 }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m[t][0], mx0), mn1 = fmaxf(m[t][1], mx1);
-            const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-            const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-            const float a0 = fast_exp2(m[t][0] - mu0), a1 = fast_exp2(m[t][1] - mu1);
-            m[t][0] = mn0;
-            m[t][1] = mn1;
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        mx0 = fmaxf(mx0, s[t][nt][e]);
+                        mx1 = fmaxf(mx1, s[t][nt][2 + e]);
+                    }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                // every row has a context token (nvalid >= 1), so mx is finite;
+                // the first block takes its maximum, later ones only raise m
+                const float d0 = fresh ? mx0 : fmaxf(mx0, 0.f);
+                const float d1 = fresh ? mx1 : fmaxf(mx1, 0.f);
+                const float a0 = fresh ? 0.f : fast_exp2(-d0);
+                const float a1 = fresh ? 0.f : fast_exp2(-d1);
+                m[t][0] += d0;
+                m[t][1] += d1;
+                l[t][0] *= a0;
+                l[t][1] *= a1;
+#pragma unroll
+                for (int n = 0; n < ND; ++n) {
+                    o[t][n][0] *= a0;
+                    o[t][n][1] *= a0;
+                    o[t][n][2] *= a1;
+                    o[t][n][3] *= a1;
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        s[t][nt][e] -= d0;
+                        s[t][nt][2 + e] -= d1;
+                    }
+            }
+            fresh = false;
+        }
+        uint32_t ph[MT][4], pl[MT][4];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
             float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    s[t][nt][e] = fast_exp2(s[t][nt][e] - mu0);
-                    s[t][nt][2 + e] = fast_exp2(s[t][nt][2 + e] - mu1);
+                    s[t][nt][e] = fast_exp2(s[t][nt][e]);
+                    s[t][nt][2 + e] = fast_exp2(s[t][nt][2 + e]);
                     ls0 += s[t][nt][e];
                     ls1 += s[t][nt][2 + e];
                 }
-            l[t][0] = l[t][0] * a0 + ls0;
-            l[t][1] = l[t][1] * a1 + ls1;
-#pragma unroll
-            for (int n = 0; n < ND; ++n) {
-                o[t][n][0] *= a0;
-                o[t][n][1] *= a0;
-                o[t][n][2] *= a1;
-                o[t][n][3] *= a1;
-            }
+            l[t][0] += ls0;
+            l[t][1] += ls1;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const float *sv = s[t][j];
@@ -191,24 +251,12 @@ struct SpMma {
                     MM::pack(sv[2] - MM::lo(ph[t][2 * j + 1]), sv[3] - MM::hi(ph[t][2 * j + 1]));
             }
         }
-        // O += P V; rows past the context may hold stale bits (even NaN): zero them
-        const bool partial = nvalid < 16;
-        const int t0 = 2 * tig;
-        const uint32_t mlo = partial ? ((t0 < nvalid ? 0x0000ffffu : 0u) |
-                                        (t0 + 1 < nvalid ? 0xffff0000u : 0u))
-                                     : 0xffffffffu;
-        const uint32_t mhi = partial ? ((t0 + 8 < nvalid ? 0x0000ffffu : 0u) |
-                                        (t0 + 9 < nvalid ? 0xffff0000u : 0u))
-                                     : 0xffffffffu;
+        // O += P V (V rows past the context were zeroed above)
         const int tok = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int np = 0; np < ND / 2; ++np) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4_trans(vaddr + swz_offset<BS>(tok, np * 2 + (lane >> 4)), b0, b1, b2, b3);
-            b0 &= mlo;
-            b2 &= mlo;
-            b1 &= mhi;
-            b3 &= mhi;
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 MM::mma(o[t][2 * np], ph[t], b0, b1);

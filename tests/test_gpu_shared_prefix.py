@@ -407,3 +407,50 @@ def test_more_than_32_parts_per_sequence():
     dw = _run(w, 64)
     assert pagedkv.get_device_error(dw.pool) == 0
     assert_close(dw.out, ref, "bf16", "64-token parts")
+
+
+# --------------------------------------------------------- climbing scores
+
+def _climbing_keys(w, rate):
+    """Scale each stored key row by 1 + rate * (its logical position), once
+    per physical block, and each new key by the factor of its position, so a
+    row's scores climb along the context: the running maximum moves many times
+    inside one work item, and many weights land just below the largest
+    stale-reference weight the kernel lets through before it rescales."""
+    BS = w.block_size
+    k = w.k_pool.float()
+    done = set()
+    for s in range(w.num_seqs):
+        c = int(w.context_lens[s])
+        for b in range(-(-c // BS)):
+            pb = int(w.block_tables[s, b])
+            if pb in done:
+                continue
+            done.add(pb)
+            f = 1.0 + rate * (b * BS + torch.arange(BS, dtype=torch.float32))
+            k[pb] *= f[None, :, None]
+    w.k_pool = k.to(w.torch_dtype)
+    f_new = 1.0 + rate * (torch.from_numpy(w.context_lens.astype(np.float32)) - 1.0)
+    w.new_key = (w.new_key.float() * f_new[:, None, None]).to(w.torch_dtype)
+    return w
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("case", ["g4_eight_members", "g8_two_items", "d64_bs32", "d256_g4",
+                                  "big_group", "varied_groups"])
+def test_shared_prefix_climbing_scores(case, dtype):
+    ctx, groups, H, Hkv, D, BS = CASES[case]
+    w = workload.build(case, dtype=dtype, context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
+                       head_dim=D, block_size=BS, data_seed=5600, meta_seed=6600, groups=groups)
+    _climbing_keys(w, rate=20.0 / max(ctx))
+    ref, _, _ = oracle_after_write(w)
+    for partition in (0, 64):
+        dw = _run(w, partition)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, dtype, f"{case} {dtype} climbing scores, partition {partition}")
+    # the plain decode on the same keys
+    dw = pagedkv.DeviceWorkload(w, out_dtype=torch.float32)
+    dw.step()
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, dtype, f"{case} {dtype} climbing scores, plain decode")
