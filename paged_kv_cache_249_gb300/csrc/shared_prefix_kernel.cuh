@@ -37,8 +37,10 @@ constexpr int kSpRows = sp_rows_for(D);
 template <int D>
 constexpr int kSpTiles = kSpRows<D> / 16;
 // Shared memory per CTA: two CTAs (8 warps) per SM, which is what the
-// register budget of the two-tile accumulators allows (a 256-wide head's
-// 16 KiB stages fit one CTA per SM).
+// register budget of the two-tile accumulators allows.  Each warp's ring
+// takes the stages that fit: two for a 128-wide head, five for a 64-wide one,
+// and one 16 KiB stage for a 256-wide head, whose eight warps per SM then hide
+// more latency than two stages for four warps would (one CTA per SM).
 constexpr int kSpSmemTarget = 112 * 1024;
 
 template <int D, int BS>
@@ -48,7 +50,7 @@ struct SpSmem {
     static constexpr int kMisc = 256;
     static constexpr int kFixed = kSpWarps * kQ + kMisc + 1024;
     static constexpr int kStagesFit = (kSpSmemTarget - kFixed) / (kSpWarps * Gm::kStageBytes);
-    static constexpr int NST = kStagesFit < 2 ? 2 : (kStagesFit > 8 ? 8 : kStagesFit);
+    static constexpr int NST = kStagesFit < 1 ? 1 : (kStagesFit > 8 ? 8 : kStagesFit);
     static constexpr int kRing = kSpWarps * NST * Gm::kStageBytes;
     static constexpr int kBars = kSpWarps * NST * 8;
     // offsets from the 1024-aligned base
