@@ -400,35 +400,49 @@ __global__ void __launch_bounds__(kSpWarps * 32)
     unsigned ctr = 0;  // blocks this warp has consumed (stage ring position, across items)
     int j0 = fetch();
     if (j0 < total) {
-        int j1 = fetch();
         SpItem it = decode(j0, field(j0));
-        int f1 = field(j1);
-        load_rows(it);
         int np = nparts_of(it);
         int ent0 = bt_load(it, 0), ent1 = bt_load(it, 1);
+        // the first stages before the query rows: every warp copies its rows
+        // at once here, and the K/V requests should not queue behind them
 #pragma unroll 1
         for (int j = 0; j < NST && j < it.nb; ++j) issue(it.g, j, __shfl_sync(FULL, ent0, j), it.b0 + j);
+        load_rows(it);
 #pragma unroll 1
         for (;;) {
             cp_async_wait_all();
             __syncwarp();  // the item's query rows are in place
-            // the item after next: index and entry; the next one: block ids and partial counts
-            const bool has_next = j1 < total;
-            const int j2 = fetch();
-            const int f2 = field(j2);
-            // (and its kv head, first block and length: its first stages go
-            // into the ring slots this item frees in its last NST blocks,
-            // since ring positions continue across items)
+            // The next item is claimed as late as its latency allows, so the
+            // longest-first list keeps balancing the warps until its end: for
+            // 128- and 256-wide heads a long item claims it three blocks before
+            // its first stage is due, reads the index a block later and
+            // decodes the entry a block after that; a short item, and every
+            // item of a 64-wide head (measured faster so, with its shorter
+            // blocks), claims it now and reads it after its first blocks.
+            // Its first stages go into the ring slots this item frees in its
+            // last NST blocks (ring positions continue across items), or
+            // after the loop if its block ids came too late.
+            const bool late = D >= 128 && it.nb > NST + 3;
+            const int claim_at = late ? it.nb - NST - 3 : -1;
+            const int read_at = late ? claim_at + 1 : 0;
+            int jn_raw = 0;
+            if (!late && lane == 0) jn_raw = atomicAdd(a.counter, 1);
+            int jn = total, fn = 0;
             int entn0 = -1, entn1 = -1, np1 = 0, nx_g = 0, nx_b0 = 0, nx_nb = 0;
-            if (has_next) {
-                const SpItem n1 = decode(j1, f1);
-                entn0 = bt_load(n1, 0);
-                entn1 = bt_load(n1, 1);
-                np1 = nparts_of(n1);
-                nx_g = n1.g;
-                nx_b0 = n1.b0;
-                nx_nb = n1.nb;
-            }
+            bool known = false;  // the next item's index and entry are decoded
+            auto learn_next = [&]() {
+                if (jn < total) {
+                    const SpItem n1 = decode(jn, fn);
+                    entn0 = bt_load(n1, 0);
+                    entn1 = bt_load(n1, 1);
+                    np1 = nparts_of(n1);
+                    nx_g = n1.g;
+                    nx_b0 = n1.b0;
+                    nx_nb = n1.nb;
+                }
+                known = true;
+            };
+            const int learn_at = late ? claim_at + 2 : (it.nb > NST ? 1 : 0);
             const bool two = it.R > 16;
             unsigned issued = ctr + min(NST, it.nb);  // ring positions issued so far
             path.reset(lane);
@@ -465,6 +479,12 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                     }
                 }
                 __syncwarp();
+                if (i == claim_at && lane == 0) jn_raw = atomicAdd(a.counter, 1);
+                if (i == read_at) {
+                    jn = __shfl_sync(FULL, jn_raw, 0);
+                    fn = field(jn);
+                }
+                if (i == learn_at) learn_next();
                 if (i + NST < it.nb) {
                     issue(it.g, kk + NST, bt_get(i + NST), it.b0 + i + NST);
                     issued = kk + NST + 1;
@@ -483,12 +503,18 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 for (unsigned kk = ctr + i; kk < issued; ++kk) mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
                 break;
             }
+            if (it.nb == 0) {  // (no block ran the loop)
+                jn = __shfl_sync(FULL, jn_raw, 0);
+                fn = field(jn);
+            }
+            if (!known) learn_next();
+            const bool has_next = jn < total;
             SpItem nx = it;
             if (has_next) {
                 // first stages the loop did not issue (all of them when this
                 // item had fewer than NST blocks), then the next query rows,
                 // before this item's epilogue
-                nx = decode(j1, f1);
+                nx = decode(jn, fn);
 #pragma unroll 1
                 for (unsigned p = issued; p < ctr + it.nb + min(NST, nx.nb); ++p) {
                     const int j = (int)(p - ctr - it.nb);
@@ -531,8 +557,6 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             }
             if (!has_next) break;
             it = nx;
-            j1 = j2;
-            f1 = f2;
             np = np1;
             ent0 = entn0;
             ent1 = entn1;
