@@ -52,7 +52,11 @@ struct SpSmem {
     static constexpr int kStagesFit = (kSpSmemTarget - kFixed) / (kSpWarps * Gm::kStageBytes);
     static constexpr int NST = kStagesFit < 1 ? 1 : (kStagesFit > 8 ? 8 : kStagesFit);
     static constexpr int kRing = kSpWarps * NST * Gm::kStageBytes;
-    static constexpr int kBars = kSpWarps * NST * 8;
+    // a one-stage ring has separate K and V barriers per stage (its K half
+    // refills while the V half is waited on and used, and the other way round)
+    static constexpr bool kSplitKV = NST == 1;
+    static constexpr int kBarsPerWarp = kSplitKV ? 2 * NST : NST;
+    static constexpr int kBars = kSpWarps * kBarsPerWarp * 8;
     // offsets from the 1024-aligned base
     static constexpr int oQ = kRing;
     static constexpr int oBars = oQ + kSpWarps * kQ;
@@ -107,22 +111,25 @@ struct SpMma {
         }
     }
 
-    // Tokens r0 .. r0+15 of the staged block (K at kaddr, V at vaddr), the
-    // first `nvalid` (1..16) of which are context tokens; query tile at qaddr.
+    // V rows r0+nvalid .. r0+15 of a partial run may hold stale bits (even
+    // NaN, and 0 * NaN is NaN): zero them in the stage before P V reads it.
+    // The fence orders these writes before the TMA refill of the slot.
+    __device__ __forceinline__ void zero_tail(uint32_t vaddr, int r0, int nvalid, int lane) {
+        constexpr int CH = D * 2 / 16;
+        for (int q = lane; q < (16 - nvalid) * CH; q += 32)
+            sts_zero16(vaddr + swz_offset<BS>(r0 + nvalid + q / CH, q % CH));
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // S = Q K^T for tokens r0 .. r0+15 of the staged K block, the first
+    // `nvalid` (1..16) of which are context tokens (query tile at qaddr), and
+    // the online softmax; P, as a high part and remainder, goes to ph / pl.
     template <int MT, int QR>
-    __device__ __forceinline__ void sub_block(uint32_t kaddr, uint32_t vaddr, uint32_t qaddr,
-                                              int r0, int nvalid, float scale_log2, int lane) {
+    __device__ __forceinline__ void scores(uint32_t kaddr, uint32_t qaddr, int r0, int nvalid,
+                                           float scale_log2, int lane, uint32_t (&ph)[MT][4],
+                                           uint32_t (&pl)[MT][4]) {
         const bool partial = nvalid < 16;  // the item's last run only (warp-uniform)
-        if (partial) {
-            // V rows past the context may hold stale bits (even NaN, and 0 * NaN
-            // is NaN): zero them in the stage before P V reads it.  The fence
-            // orders these writes before the TMA refill of the slot.
-            constexpr int CH = D * 2 / 16;
-            for (int q = lane; q < (16 - nvalid) * CH; q += 32)
-                sts_zero16(vaddr + swz_offset<BS>(r0 + nvalid + q / CH, q % CH));
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
         float s[MT][2][4];
 #pragma unroll
         for (int t = 0; t < MT; ++t)
@@ -228,7 +235,6 @@ struct SpMma {
             }
             fresh = false;
         }
-        uint32_t ph[MT][4], pl[MT][4];
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
             float ls0 = 0.f, ls1 = 0.f;
@@ -253,7 +259,13 @@ struct SpMma {
                     MM::pack(sv[2] - MM::lo(ph[t][2 * j + 1]), sv[3] - MM::hi(ph[t][2 * j + 1]));
             }
         }
-        // O += P V (V rows past the context were zeroed above)
+    }
+
+    // O += P V for the same tokens of the staged V block (rows past the
+    // context zeroed first).
+    template <int MT>
+    __device__ __forceinline__ void accumulate(uint32_t vaddr, int r0, int lane,
+                                               const uint32_t (&ph)[MT][4], const uint32_t (&pl)[MT][4]) {
         const int tok = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int np = 0; np < ND / 2; ++np) {
@@ -270,6 +282,18 @@ struct SpMma {
                 MM::mma(o[t][2 * np + 1], pl[t], b2, b3);
             }
         }
+    }
+
+    // Both, for tokens r0 .. r0+15 of a block staged whole (K at kaddr, V at
+    // vaddr); the stale V rows are zeroed first, so the writes overlap the
+    // arithmetic.
+    template <int MT, int QR>
+    __device__ __forceinline__ void sub_block(uint32_t kaddr, uint32_t vaddr, uint32_t qaddr,
+                                              int r0, int nvalid, float scale_log2, int lane) {
+        if (nvalid < 16) zero_tail(vaddr, r0, nvalid, lane);
+        uint32_t ph[MT][4], pl[MT][4];
+        scores<MT, QR>(kaddr, qaddr, r0, nvalid, scale_log2, lane, ph, pl);
+        accumulate<MT>(vaddr, r0, lane, ph, pl);
     }
 
     // query buffer of QR rows (32: two tiles for a prefix item; 16: one warp's own)
@@ -303,11 +327,13 @@ __global__ void __launch_bounds__(kSpWarps * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = a.num_kv_heads, G = a.group;
     unsigned char *wstage = smem + warp * NST * Gm::kStageBytes;
-    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + Sm::oBars) + warp * NST;
+    constexpr bool kSplit = Sm::kSplitKV;
+    static_assert(!kSplit || BS == 16, "split K/V ring: 16-row runs");
+    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + Sm::oBars) + warp * Sm::kBarsPerWarp;
     const uint32_t qaddr = smem_u32(smem + Sm::oQ + warp * Sm::kQ);
     if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < NST; ++i) mbar_init(&wbar[i], 1);
+        for (int i = 0; i < Sm::kBarsPerWarp; ++i) mbar_init(&wbar[i], 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
@@ -358,7 +384,31 @@ __global__ void __launch_bounds__(kSpWarps * 32)
     };
     // stage run `run` (of its sequence) of block pb at absolute ring position k
     const uint64_t kv_policy = l2_evict_first_policy();  // K/V tiles are read once
+    // one half (0: K, 1: V) of the stage at ring position k of a split ring,
+    // on its own barrier (K barriers first, then V barriers)
+    auto issue_half = [&](int h, int g, unsigned k, int pb, int run) {
+        if (lane == 0) {
+            uint64_t *bar = &wbar[h * NST + k % NST];
+            if (pb >= 0 && pb < a.num_blocks) {
+                mbar_arrive_expect_tx(bar, Gm::kTileBytes);
+                unsigned char *dst = wstage + (k % NST) * Gm::kStageBytes + h * Gm::kTileBytes;
+                const int y = (((pb * Hkv + g) << ushift) + (run & ((1 << ushift) - 1))) * BS;
+#pragma unroll
+                for (int sl = 0; sl < Gm::kSlabs; ++sl)
+                    tma_load_2d_hint(dst + sl * Gm::kSlabBytes, h ? &tmv : &tmk, sl * Gm::kSlabElems, y,
+                                     bar, kv_policy);
+            } else {
+                raise_fault(a.dev_error, PKV_FAULT_BLOCK_ID);
+                mbar_arrive(bar);
+            }
+        }
+    };
     auto issue = [&](int g, unsigned k, int pb, int run) {
+        if constexpr (kSplit) {
+            issue_half(0, g, k, pb, run);
+            issue_half(1, g, k, pb, run);
+            return;
+        }
         if (lane == 0) {
             uint64_t *bar = &wbar[k % NST];
             if (pb >= 0 && pb < a.num_blocks) {
@@ -445,6 +495,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             const int learn_at = late ? claim_at + 2 : (it.nb > NST ? 1 : 0);
             const bool two = it.R > 16;
             unsigned issued = ctr + min(NST, it.nb);  // ring positions issued so far
+            unsigned issued_k = issued;               // (K halves, for a split ring)
             path.reset(lane);
             int cb = 0;
             bool ok = true;
@@ -461,6 +512,66 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 }
                 const int pb = bt_get(i);
                 const unsigned kk = ctr + i;
+                if constexpr (kSplit) {
+                    // K half: scores; then the K half of position kk + NST
+                    // (this item's block i + NST, or the next item's block j,
+                    // in order) goes into the freed slot while the V half is
+                    // waited on and used
+                    ok = __all_sync(FULL, mbar_wait(&wbar[kk % NST], (kk / NST) & 1));
+                    if (!ok) break;
+                    const bool valid = pb >= 0 && pb < a.num_blocks;
+                    const int nvalid = min(BS, it.tok_end - (it.b0 + i) * BS);
+                    const uint32_t kaddr = smem_u32(wstage + (kk % NST) * Gm::kStageBytes);
+                    const uint32_t vaddr = kaddr + Gm::kTileBytes;
+                    uint32_t ph[2][4], pl[2][4];
+                    auto &ph1 = reinterpret_cast<uint32_t(&)[1][4]>(ph);
+                    auto &pl1 = reinterpret_cast<uint32_t(&)[1][4]>(pl);
+                    if (valid) {
+                        if (kSpTiles<D> == 2 && two)
+                            path.template scores<2, kSpRows<D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph, pl);
+                        else
+                            path.template scores<1, kSpRows<D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph1, pl1);
+                    }
+                    int ng = -1, npb = -1, nrun = 0;
+                    if (i + NST < it.nb) {
+                        ng = it.g;
+                        npb = bt_get(i + NST);
+                        nrun = it.b0 + i + NST;
+                    } else if (it.nb >= NST && issued == kk + NST && i + NST - it.nb < nx_nb) {
+                        // (only if every earlier position is issued: a next
+                        // item learnt late takes its first stages after the loop)
+                        const int j = i + NST - it.nb;  // < NST: within the first 32 entries
+                        ng = nx_g;
+                        npb = __shfl_sync(FULL, entn0, j);
+                        nrun = nx_b0 + j;
+                    }
+                    __syncwarp();  // every lane's K fragments are read
+                    if (ng >= 0) {
+                        issue_half(0, ng, kk + NST, npb, nrun);
+                        issued_k = kk + NST + 1;
+                    }
+                    ok = __all_sync(FULL, mbar_wait(&wbar[NST + kk % NST], (kk / NST) & 1));
+                    if (!ok) break;
+                    if (valid) {
+                        if (nvalid < 16) path.zero_tail(vaddr, 0, nvalid, lane);
+                        if (kSpTiles<D> == 2 && two)
+                            path.template accumulate<2>(vaddr, 0, lane, ph, pl);
+                        else
+                            path.template accumulate<1>(vaddr, 0, lane, ph1, pl1);
+                    }
+                    __syncwarp();
+                    if (i == claim_at && lane == 0) jn_raw = atomicAdd(a.counter, 1);
+                    if (i == read_at) {
+                        jn = __shfl_sync(FULL, jn_raw, 0);
+                        fn = field(jn);
+                    }
+                    if (i == learn_at) learn_next();
+                    if (ng >= 0) {
+                        issue_half(1, ng, kk + NST, npb, nrun);
+                        issued = kk + NST + 1;
+                    }
+                    continue;
+                }
                 ok = __all_sync(FULL, mbar_wait(&wbar[kk % NST], (kk / NST) & 1));
                 if (!ok) break;
                 if (pb >= 0 && pb < a.num_blocks) {
@@ -500,7 +611,12 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             if (!ok) {
                 if (lane == 0) raise_fault(a.dev_error, PKV_FAULT_TIMEOUT);
                 // drain what this warp still has in flight, again with a bound
-                for (unsigned kk = ctr + i; kk < issued; ++kk) mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
+                if constexpr (kSplit) {
+                    for (unsigned kk = ctr + i; kk < issued_k; ++kk) mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
+                    for (unsigned kk = ctr + i; kk < issued; ++kk) mbar_wait(&wbar[NST + kk % NST], (kk / NST) & 1);
+                } else {
+                    for (unsigned kk = ctr + i; kk < issued; ++kk) mbar_wait(&wbar[kk % NST], (kk / NST) & 1);
+                }
                 break;
             }
             if (it.nb == 0) {  // (no block ran the loop)
