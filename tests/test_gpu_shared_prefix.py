@@ -454,3 +454,53 @@ def test_shared_prefix_climbing_scores(case, dtype):
     torch.cuda.synchronize()
     assert pagedkv.get_device_error(dw.pool) == 0
     assert_close(dw.out, ref, dtype, f"{case} {dtype} climbing scores, plain decode")
+
+
+# ------------------------------------------- faults and short items, all rings
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_shared_prefix_bad_block_id_sets_fault_and_spares_other_sequences(D):
+    """A block id outside the pool in one member's own blocks: the kernel's
+    bound check reports it and skips the block (for a 256-wide head the K and
+    V halves of its one-stage ring are released separately); every sequence
+    that does not name the block is still exact."""
+    ctx = _prefix_ctx(64, [40, 70, 5, 100])
+    w = _w(f"badblk{D}", ctx, [(4, 64)], 16, 4, D, 16, seed=900 + D)
+    ref, _, _ = oracle_after_write(w)
+    dw = pagedkv.DeviceWorkload(w, out_dtype=torch.float32)
+    pagedkv.reshape_and_cache(dw.pool, dw.new_key, dw.new_value, dw.slot_mapping)
+    bt = w.block_tables
+    bad_seq, bad_blk = 1, 5  # past the 4-block prefix: sequence 1's own block
+    assert bt[bad_seq, bad_blk] >= 0 and not np.any(np.delete(bt, bad_seq, 0) == bt[bad_seq, bad_blk])
+    dw.block_tables[bad_seq, bad_blk] = w.num_blocks + 7
+    dw.shared_prefix_setup()
+    dw.decode_shared_prefix()
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dw.pool) == pagedkv.FAULT_BLOCK_ID
+    out = dw.out.cpu()
+    assert torch.isfinite(out).all()
+    for s in range(w.num_seqs):
+        if s != bad_seq:
+            assert_close(out[s], ref[s], "bf16", f"D{D}: unaffected sequence {s}")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_shared_prefix_many_short_items(D):
+    """Only items of one to three blocks, many per warp: each item is shorter
+    than the lead the next item's claim needs, so the next item's first stages
+    are requested after the current one's loop, item after item."""
+    rng = np.random.default_rng(77 + D)
+    groups, ctx = [], []
+    for _ in range(150):
+        members = int(rng.integers(1, 4))
+        prefix = 16 * int(rng.integers(1, 3)) if members > 1 else 0
+        groups.append((members, prefix))
+        ctx += [prefix + int(rng.integers(1, 48)) for _ in range(members)]
+    w = workload.build(f"short{D}", dtype="bf16", context_lens=ctx, num_heads=8, num_kv_heads=2,
+                       head_dim=D, block_size=16, data_seed=7700 + D, meta_seed=7800 + D,
+                       groups=groups)
+    ref, _, _ = oracle_after_write(w)
+    for partition in (0, 16):
+        dw = _run(w, partition)
+        assert pagedkv.get_device_error(dw.pool) == 0
+        assert_close(dw.out, ref, "bf16", f"D{D} short items, partition {partition}")
