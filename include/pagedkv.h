@@ -286,8 +286,8 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * multiple of block_size, at most 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: BF16 or F16
- * pools (head_dim 64, 128 or 256; a 256-wide head's work items carry 16
- * query rows instead of 32), num_heads / num_kv_heads in 1..16, out_dtype
+ * pools (head_dim 64, 128 or 256; the work items of 64- and 256-wide heads
+ * carry 16 query rows instead of 32), num_heads / num_kv_heads in 1..16, out_dtype
  * F32, BF16 or F16.
  */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,

@@ -17,8 +17,11 @@ constexpr int kMaxGroup = 16;
 constexpr int kMaxStageRows = 16;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 // Query rows of a shared-prefix work item for a head size: two 16-row tiles
-// up to 128 columns, one tile of a 256-wide head (the same accumulator registers).
-constexpr int sp_rows_for(int head_dim) { return head_dim > 128 ? 16 : kSpRowsMax; }
+// for a 128-wide head; one tile for a 256-wide head (the same accumulator
+// registers) and for a 64-wide one, whose lighter items then fit four CTAs
+// per SM (measured faster than two CTAs of two-tile items, although a group
+// with more members than one item holds reads its prefix once per item).
+constexpr int sp_rows_for(int head_dim) { return head_dim == 128 ? kSpRowsMax : 16; }
 
 // Arguments of one decode launch; every pointer is a device pointer.
 struct DecodeArgs {

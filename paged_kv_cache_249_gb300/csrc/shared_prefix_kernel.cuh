@@ -9,7 +9,7 @@
 // then needs to come from HBM once for the whole group, not once per
 // sequence: a "prefix item" stages a block once and multiplies it against
 // the query rows of every member (members x GQA group <= 32 rows, two 16-row
-// mma.sync tiles; 16 rows, one tile, for a 256-wide head), while "suffix
+// mma.sync tiles; 16 rows, one tile, for 64- and 256-wide heads), while "suffix
 // items" walk each sequence's own blocks.
 // Every item leaves a normalised partial output and its log2-sum-exp per
 // query row (or the final row when it is the sequence's only part); the
@@ -36,12 +36,14 @@ template <int D>
 constexpr int kSpRows = sp_rows_for(D);
 template <int D>
 constexpr int kSpTiles = kSpRows<D> / 16;
-// Shared memory per CTA: two CTAs (8 warps) per SM, which is what the
-// register budget of the two-tile accumulators allows.  Each warp's ring
-// takes the stages that fit: two for a 128-wide head, five for a 64-wide one,
-// and one 16 KiB stage for a 256-wide head, whose eight warps per SM then hide
-// more latency than two stages for four warps would (one CTA per SM).
-constexpr int kSpSmemTarget = 112 * 1024;
+// Shared memory per CTA: two CTAs (8 warps) per SM for 128- and 256-wide
+// heads, which is what the register budget of their accumulators allows, and
+// four CTAs (16 warps) for the one-tile items of a 64-wide head.  Each warp's
+// ring takes the stages that fit: two for a 128-wide head, two for a 64-wide
+// one, and one 16 KiB stage for a 256-wide head, whose eight warps per SM then
+// hide more latency than two stages for four warps would (one CTA per SM).
+template <int D>
+constexpr int kSpSmemTarget = D == 64 ? 55 * 1024 : 112 * 1024;
 
 template <int D, int BS>
 struct SpSmem {
@@ -49,7 +51,7 @@ struct SpSmem {
     static constexpr int kQ = kSpRows<D> * D * 2;  // a warp's query rows (16-bit, swizzled slabs)
     static constexpr int kMisc = 256;
     static constexpr int kFixed = kSpWarps * kQ + kMisc + 1024;
-    static constexpr int kStagesFit = (kSpSmemTarget - kFixed) / (kSpWarps * Gm::kStageBytes);
+    static constexpr int kStagesFit = (kSpSmemTarget<D> - kFixed) / (kSpWarps * Gm::kStageBytes);
     static constexpr int NST = kStagesFit < 1 ? 1 : (kStagesFit > 8 ? 8 : kStagesFit);
     static constexpr int kRing = kSpWarps * NST * Gm::kStageBytes;
     // a one-stage ring has separate K and V barriers per stage (its K half

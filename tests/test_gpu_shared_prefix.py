@@ -218,10 +218,11 @@ def test_run_without_or_against_another_plan_is_reported():
 
 def _expected_items(w, pbp, pbs):
     """Work items of the group description, derived on the host: per group
-    with a shared prefix, ceil(members / floor(32 / G)) row sets x the prefix
-    parts; per sequence, its own blocks after the prefix in parts of pbs."""
+    with a shared prefix, ceil(members / floor(R / G)) row sets x the prefix
+    parts (R = 32 query rows per item for a 128-wide head, 16 otherwise); per
+    sequence, its own blocks after the prefix in parts of pbs."""
     BS, G = w.block_size, w.num_heads // w.num_kv_heads
-    mpi = 32 // G
+    mpi = (32 if w.head_dim == 128 else 16) // G
     gs, gp = w.groups()
     ctx = np.asarray(w.context_lens)
     pre, suf = [], []
