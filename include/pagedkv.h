@@ -258,10 +258,11 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * search; the Hacker News thread on PagedAttention describes such sharing of
  * blocks between a sequence's siblings, and Qualiteg's "About PagedAttention
  * for LLM serving" the per-sequence block tables that make it possible).
- * Each shared block is read from HBM once per kv head for the whole group and
- * multiplied against every member's query rows on tensor cores; each
- * member's own blocks after the prefix are read as usual; a log-sum-exp pass
- * merges the parts.
+ * Each shared block is staged once per kv head for up to 32 query rows of
+ * the group (16 for 64- and 256-wide heads; a larger group stages it once per
+ * such set of rows, the repeats mostly from L2) and multiplied against those
+ * members' query rows on tensor cores; each member's own blocks after the
+ * prefix are read as usual; a log-sum-exp pass merges the parts.
  *
  * Groups: group i is sequences group_starts[i] .. group_starts[i+1]-1, and
  * every member's first prefix_lens[i] / block_size block-table entries name
