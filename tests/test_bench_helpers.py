@@ -83,3 +83,15 @@ def test_shared_prefix_shapes_the_bench_routes(bench):
     assert not bench.shared_prefix_supported(w)  # fp32 pools take the plain decode
     w16 = workload.make("tiny_f32", dtype="bf16", head_dim=128)
     assert bench.shared_prefix_supported(w16)
+
+
+def test_kernel_source_lists_name_existing_files(bench):
+    """The files whose hash dates each stored DRAM-traffic record exist, and
+    the hash is a function of their contents alone."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_249_gb300", "csrc")
+    for family, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.isfile(os.path.join(csrc, f)), (family, f)
+        assert bench.kernel_source_hash(family) == bench.kernel_source_hash(family)
+    for (name, family), rec in bench.NCU_TRAFFIC.items():
+        assert family in bench.KERNEL_SOURCES and rec["bytes"] > 0 and len(rec["src"]) == 16
