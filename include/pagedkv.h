@@ -69,7 +69,8 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
 
 /* Flags of pkv_paged_attention_decode. */
 #define PKV_DECODE_PATH_AUTO 0  /* tensor cores when the GQA group makes dense tiles */
-#define PKV_DECODE_PATH_FMA 1   /* CUDA-core dot products for every group size */
+#define PKV_DECODE_PATH_FMA 1   /* CUDA-core dot products for every group size (groups above
+                                   4 rows are split over CTAs of the same kv head) */
 #define PKV_DECODE_PATH_MMA 2   /* tensor-core tiles (bf16 or fp16 pools) for every group size */
 
 /*

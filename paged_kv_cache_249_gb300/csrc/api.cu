@@ -295,6 +295,9 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     a.num_heads = num_heads;
     a.num_kv_heads = num_kv_heads;
     a.group = group;
+    // the CUDA-core path takes at most kFmaRowsMax rows of a group per CTA
+    a.row_split = mma ? 1 : (group + kFmaRowsMax - 1) / kFmaRowsMax;
+    a.rows_per_cta = (group + a.row_split - 1) / a.row_split;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = pool->num_blocks;
     a.ctx_cap = ctx_cap;
@@ -306,8 +309,9 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     // the tensor-core kernel of a 256-wide head holds 254 registers a thread:
     // two CTAs per SM instead of three
     const int ctas_per_sm = (pool->head_dim == 256 && mma) ? 2 : 3;
-    const int pt = resolve_partition(partition_tokens, ctx_cap, (long long)num_seqs * num_kv_heads,
-                                     sm_count(dev), ctas_per_sm);
+    const int pt = resolve_partition(partition_tokens, ctx_cap,
+                                     (long long)num_seqs * num_kv_heads * a.row_split, sm_count(dev),
+                                     ctas_per_sm);
     int parts = 1;
     if (pt > 0) {
         a.part_blocks = pt / U;
@@ -340,7 +344,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     L.block_size = U;
     L.runs = unit_shift > 0;
     int gp = 1;
-    while (gp < group) gp <<= 1;
+    while (gp < a.rows_per_cta) gp <<= 1;
     L.group_pad = gp;
     L.mma = mma;
     L.stream = static_cast<cudaStream_t>(stream);

@@ -481,8 +481,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-    // kv head fastest: consecutive CTAs read neighbouring (block, kv head) tiles
-    const int g = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+    // kv head fastest: consecutive CTAs read neighbouring (block, kv head)
+    // tiles; a group split over row_split CTAs has them side by side
+    const int g = blockIdx.x / a.row_split, s = blockIdx.y, part = blockIdx.z;
+    const int r0 = (blockIdx.x - g * a.row_split) * a.rows_per_cta;  // first query row of the group
+    const int nrows = min(a.rows_per_cta, a.group - r0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     griddep_wait();  // inputs written by the kernel before this one are complete
 
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     int ctx = __ldg(a.context_lens + s);
     if (ctx < 0 || ctx > a.ctx_cap) {
-        if (threadIdx.x == 0 && g == 0 && part == 0) raise_fault(a.dev_error, PKV_FAULT_CONTEXT);
+        if (threadIdx.x == 0 && blockIdx.x == 0 && part == 0) raise_fault(a.dev_error, PKV_FAULT_CONTEXT);
         ctx = ctx < 0 ? 0 : a.ctx_cap;
     }
     const int nblk = (ctx + BS - 1) / BS;
@@ -558,8 +561,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     Path path;
     const T *qrow0 = reinterpret_cast<const T *>(a.q) +
-                     ((size_t)s * a.num_heads + (size_t)g * a.group) * D;
-    path.init(qrow0, a.group, a.scale_log2, lane);
+                     ((size_t)s * a.num_heads + (size_t)g * a.group + r0) * D;
+    path.init(qrow0, nrows, a.scale_log2, lane);
 
 #pragma unroll 1
     for (int i = 0; i < NST && i < nw; ++i) issue(i, bt_get(i));
@@ -600,9 +603,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     path.finish(&states[warp], lane);
     __syncthreads();
 
-    const int G = a.group;
+    const int G = nrows;  // this CTA's rows of the group
     const bool split = nparts > 1;
-    const size_t head0 = (size_t)s * a.num_heads + (size_t)g * G;
+    const size_t head0 = (size_t)s * a.num_heads + (size_t)g * a.group + r0;
 #pragma unroll 1
     for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int r = idx / D, d = idx % D;
@@ -650,7 +653,7 @@ pkv_status launch_one(const DecodeLaunch &L) {
             return PKV_ERR_CUDA;
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
     }
-    dim3 grid(L.args.num_kv_heads, L.num_seqs, L.args.num_parts);
+    dim3 grid(L.args.num_kv_heads * L.args.row_split, L.num_seqs, L.args.num_parts);
     return cuda_status(
         launch_dependent(kern, grid, dim3(kDecodeWarps * 32), smem, L.stream, *L.tmk, *L.tmv, L.args));
 }

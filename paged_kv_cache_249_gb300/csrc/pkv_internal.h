@@ -14,6 +14,12 @@ constexpr uint32_t kPoolMagic = 0x504b5631u;  // "PKV1"
 constexpr int kAutoPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 8192;
 constexpr int kMaxGroup = 16;
+// CUDA-core decode: query rows of a group one CTA takes at most.  A larger
+// group is split over CTAs of the same kv head, launched side by side so the
+// repeated reads of each K/V tile mostly hit L2: each thread holds its slice
+// of every row's query and accumulator, and 16 rows spilled (fp32, G = 16:
+// 0.14 of the copy peak whole, 0.38 in CTAs of 8 rows, 0.40 in CTAs of 4)
+constexpr int kFmaRowsMax = 4;
 constexpr int kMaxStageRows = 16;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 // Query rows of a shared-prefix work item for a head size: two 16-row tiles
@@ -35,6 +41,8 @@ struct DecodeArgs {
     int num_heads;
     int num_kv_heads;
     int group;                  // num_heads / num_kv_heads
+    int row_split;              // CTAs per kv head, each with its own query rows of the group
+    int rows_per_cta;           // ceil(group / row_split)
     int max_blocks_per_seq;
     int num_blocks;
     int ctx_cap;                // min(max_blocks_per_seq * BS, max_context_len)
