@@ -307,15 +307,17 @@ struct MmaPath {
 
     uint32_t qa[KS][4];                 // A fragments of Q (rows g, g+8)
     float o[ND][4];                     // O accumulators (rows g, g+8)
-    float m0, m1, l0, l1;               // rows g and g+8; l is lane-partial
+    float m0, m1, l0, l1;               // rows g and g+8: reference, lane-partial sum
     float scale_log2;
     int gid, tig;
+    bool fresh;                         // no block seen yet
 
     __device__ __forceinline__ void init(const T *qrow0, int group, float sl2, int lane) {
         gid = lane >> 2;
         tig = lane & 3;
         scale_log2 = sl2;
-        m0 = m1 = -CUDART_INF_F;
+        fresh = true;
+        m0 = m1 = 0.f;
         l0 = l1 = 0.f;
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow0);
 #pragma unroll
@@ -344,48 +346,74 @@ struct MmaPath {
                 MM::mma(s[nt], qa[2 * kc + 1], b2, b3);
             }
         }
-        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+        // lazy reference: m moves (and l, o are rescaled) only when a score
+        // passes it by more than 8 (log2 units); weights stay at most 2^8
+        if (nvalid < BS) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    if (nt * 8 + 2 * tig + e >= nvalid) s[nt][e] = s[nt][2 + e] = -CUDART_INF_F;
+        }
+        bool grow = fresh;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const bool ok = nt * 8 + 2 * tig + e < nvalid;
-                s[nt][e] = ok ? s[nt][e] * scale_log2 : -CUDART_INF_F;
-                s[nt][2 + e] = ok ? s[nt][2 + e] * scale_log2 : -CUDART_INF_F;
-                mx0 = fmaxf(mx0, s[nt][e]);
-                mx1 = fmaxf(mx1, s[nt][2 + e]);
+                s[nt][e] = fmaf(s[nt][e], scale_log2, -m0);
+                s[nt][2 + e] = fmaf(s[nt][2 + e], scale_log2, -m1);
+                grow |= s[nt][e] > 8.f;
+                grow |= s[nt][2 + e] > 8.f;
             }
         }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-        const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-        const float a0 = fast_exp2(m0 - mu0), a1 = fast_exp2(m1 - mu1);
-        m0 = mn0;
-        m1 = mn1;
+        if (__any_sync(0xffffffffu, grow)) {
+            float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mx0 = fmaxf(mx0, s[nt][e]);
+                    mx1 = fmaxf(mx1, s[nt][2 + e]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float d0 = fresh ? mx0 : fmaxf(mx0, 0.f), d1 = fresh ? mx1 : fmaxf(mx1, 0.f);
+            const float a0 = fresh ? 0.f : fast_exp2(-d0), a1 = fresh ? 0.f : fast_exp2(-d1);
+            m0 += d0;
+            m1 += d1;
+            l0 *= a0;
+            l1 *= a1;
+#pragma unroll
+            for (int n = 0; n < ND; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    s[nt][e] -= d0;
+                    s[nt][2 + e] -= d1;
+                }
+            fresh = false;
+        }
         float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                s[nt][e] = fast_exp2(s[nt][e] - mu0);
-                s[nt][2 + e] = fast_exp2(s[nt][2 + e] - mu1);
+                s[nt][e] = fast_exp2(s[nt][e]);
+                s[nt][2 + e] = fast_exp2(s[nt][2 + e]);
                 ls0 += s[nt][e];
                 ls1 += s[nt][2 + e];
             }
         }
-        l0 = l0 * a0 + ls0;
-        l1 = l1 * a1 + ls1;
-#pragma unroll
-        for (int n = 0; n < ND; ++n) {
-            o[n][0] *= a0;
-            o[n][1] *= a0;
-            o[n][2] *= a1;
-            o[n][3] *= a1;
-        }
+        l0 += ls0;
+        l1 += ls1;
 #pragma unroll
         for (int kt = 0; kt < BS / 16; ++kt) {
             // P as A fragments: its 16-bit high part and the 16-bit remainder
@@ -441,10 +469,11 @@ struct MmaPath {
             }
         }
         if (tig == 0) {
-            st->m[gid] = m0;
+            // a warp that saw no block has no reference: it must not set M
+            st->m[gid] = fresh ? -CUDART_INF_F : m0;
             st->l[gid] = l0;
             if constexpr (RG == 16) {
-                st->m[gid + 8] = m1;
+                st->m[gid + 8] = fresh ? -CUDART_INF_F : m1;
                 st->l[gid + 8] = l1;
             }
         }
