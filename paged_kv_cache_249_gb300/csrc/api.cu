@@ -264,11 +264,12 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     const int group = num_heads / num_kv_heads;
     if (group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
     if (num_kv_heads > 65535 || num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid y
-    const bool half16 = pool->dtype != PKV_F32;  // bf16 or fp16: tensor-core tiles possible
-    bool mma = half16 && group >= 4;
+    const bool half16 = pool->dtype != PKV_F32;  // bf16 or fp16: 16-bit tensor-core tiles
+    // fp32 storage takes TF32 tiles (three products each) for the larger groups
+    bool mma = half16 ? group >= 4 : group >= kTf32MinGroup;
     if (flags == PKV_DECODE_PATH_FMA) mma = false;
     if (flags == PKV_DECODE_PATH_MMA) {
-        if (!half16) return PKV_ERR_UNSUPPORTED;
+        if (!half16 && pool->head_dim > 128) return PKV_ERR_UNSUPPORTED;
         mma = true;
     }
     int dev = 0;
@@ -306,9 +307,11 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     a.unit_shift = unit_shift;
     a.scale_log2 = scale * 1.4426950408889634f;
 
-    // the tensor-core kernel of a 256-wide head holds 254 registers a thread:
-    // two CTAs per SM instead of three
-    const int ctas_per_sm = (pool->head_dim == 256 && mma) ? 2 : 3;
+    // the tensor-core kernels of a 256-wide head (16-bit storage) and of a
+    // 128-wide head (fp32 storage, TF32) hold ~255 registers a thread: two
+    // CTAs per SM instead of three
+    const int ctas_per_sm =
+        (mma && (pool->head_dim == 256 || (!half16 && pool->head_dim == 128))) ? 2 : 3;
     const int pt = resolve_partition(partition_tokens, ctx_cap,
                                      (long long)num_seqs * num_kv_heads * a.row_split, sm_count(dev),
                                      ctas_per_sm);

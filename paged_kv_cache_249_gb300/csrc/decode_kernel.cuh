@@ -480,6 +480,245 @@ struct MmaPath {
     }
 };
 
+// ------------------------------------------------------ TF32 tensor cores
+
+// fp32 value rounded to TF32 (10-bit mantissa, nearest, ties away), as the
+// 32-bit operand register of a TF32 MMA.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// x as a TF32 high part and the TF32 rounding of its remainder
+__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
+}
+
+// D = A(16x8 tf32, row) * B(8x8 tf32, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// a*b to about fp32 accuracy from three TF32 products: hi*hi + hi*lo + lo*hi
+// (the lo*lo term is below 2^-22 of the product)
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const uint32_t (&ah)[4],
+                                           const uint32_t (&al)[4], uint32_t bh0, uint32_t bh1,
+                                           uint32_t bl0, uint32_t bl1) {
+    mma_tf32_1688(d, al, bh0, bh1);
+    mma_tf32_1688(d, ah, bl0, bl1);
+    mma_tf32_1688(d, ah, bh0, bh1);
+}
+
+// fp32 storage on tensor cores: the G query rows (padded to 16) as m16n8k8
+// TF32 tiles, each product taken as three TF32 products so that scores and
+// outputs keep about fp32 accuracy.  K fragments come from the swizzled
+// stage with ldmatrix (an 8-row, 16-byte matrix of the 16-bit view holds an
+// 8x4 block of fp32, one value per lane, which is what a TF32 B fragment
+// wants); V fragments with 16-byte loads, four O columns at a time, so O's
+// columns inside each 32-column group are permuted (column d = 32g + 4n + j
+// is n-tile j's column n) and restored when the warp exports its state.
+template <int D, int BS, int RG>
+struct Tf32Path {
+    static constexpr int KS = D / 8;   // k-steps of the QK^T product
+    static constexpr int NT = BS / 8;  // token n-tiles per block (k-steps of P V)
+    static constexpr int NG = D / 32;  // 32-column groups of O
+    static_assert(BS == 16 && D % 32 == 0, "tile shape");
+
+    uint32_t qh[KS][4], ql[KS][4];  // A fragments of Q (rows g, g+8): high part and remainder
+    float o[NG][4][4];              // O accumulators: column group, n-tile, C fragment
+    float m0, m1, l0, l1;           // rows g and g+8: reference, lane-partial sum
+    float scale_log2;
+    int gid, tig;
+    bool fresh;                     // no block seen yet
+
+    __device__ __forceinline__ void init(const float *qrow0, int group, float sl2, int lane) {
+        gid = lane >> 2;
+        tig = lane & 3;
+        scale_log2 = sl2;
+        fresh = true;
+        m0 = m1 = 0.f;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int c0 = ks * 8 + tig, c1 = c0 + 4;
+            const float x0 = gid < group ? __ldg(qrow0 + (size_t)gid * D + c0) : 0.f;
+            const float x1 = gid + 8 < group ? __ldg(qrow0 + (size_t)(gid + 8) * D + c0) : 0.f;
+            const float x2 = gid < group ? __ldg(qrow0 + (size_t)gid * D + c1) : 0.f;
+            const float x3 = gid + 8 < group ? __ldg(qrow0 + (size_t)(gid + 8) * D + c1) : 0.f;
+            tf32_split(x0, qh[ks][0], ql[ks][0]);
+            tf32_split(x1, qh[ks][1], ql[ks][1]);
+            tf32_split(x2, qh[ks][2], ql[ks][2]);
+            tf32_split(x3, qh[ks][3], ql[ks][3]);
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[g][j][0] = o[g][j][1] = o[g][j][2] = o[g][j][3] = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t kaddr, uint32_t vaddr, int nvalid, int lane) {
+        // S = Q K^T: lane L names row (L & 7) of matrix L >> 3 of an ldmatrix.x4
+        // whose matrices are (tokens 0-7 | 8-15) x (head columns 8ks..+3 | +4..+7)
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        const int ktok = (lane >> 4) * 8 + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t r[4];
+            ldsm_x4(kaddr + swz_offset<BS>(ktok, ks * 2 + ((lane >> 3) & 1)), r[0], r[1], r[2], r[3]);
+            uint32_t kh[4], kl[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tf32_split(__uint_as_float(r[i]), kh[i], kl[i]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_tf32x3(s[nt], qh[ks], ql[ks], kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
+        }
+        // online softmax against a lazy reference (as on the 16-bit path)
+        if (nvalid < BS) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    if (nt * 8 + 2 * tig + e >= nvalid) s[nt][e] = s[nt][2 + e] = -CUDART_INF_F;
+        }
+        bool grow = fresh;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                s[nt][e] = fmaf(s[nt][e], scale_log2, -m0);
+                s[nt][2 + e] = fmaf(s[nt][2 + e], scale_log2, -m1);
+                grow |= s[nt][e] > 8.f;
+                grow |= s[nt][2 + e] > 8.f;
+            }
+        if (__any_sync(0xffffffffu, grow)) {
+            float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mx0 = fmaxf(mx0, s[nt][e]);
+                    mx1 = fmaxf(mx1, s[nt][2 + e]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float d0 = fresh ? mx0 : fmaxf(mx0, 0.f), d1 = fresh ? mx1 : fmaxf(mx1, 0.f);
+            const float a0 = fresh ? 0.f : fast_exp2(-d0), a1 = fresh ? 0.f : fast_exp2(-d1);
+            m0 += d0;
+            m1 += d1;
+            l0 *= a0;
+            l1 *= a1;
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    o[g][j][0] *= a0;
+                    o[g][j][1] *= a0;
+                    o[g][j][2] *= a1;
+                    o[g][j][3] *= a1;
+                }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    s[nt][e] -= d0;
+                    s[nt][2 + e] -= d1;
+                }
+            fresh = false;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[nt][e] = fast_exp2(s[nt][e]);
+                (e < 2 ? l0 : l1) += s[nt][e];
+            }
+        // O += P V, one 8-token k-step per n-tile of S.  P moves from the C
+        // layout (row g, columns 2t, 2t+1) to the A layout (row g, columns t,
+        // t+4) by shuffles inside each group of four lanes.
+        const int base = lane & ~3, srcA = base + (tig >> 1), srcB = srcA + 2;
+        const bool odd = tig & 1;
+#pragma unroll
+        for (int kt = 0; kt < NT; ++kt) {
+            float pa[4];
+            {
+                const float x0 = __shfl_sync(0xffffffffu, s[kt][0], srcA);
+                const float x1 = __shfl_sync(0xffffffffu, s[kt][1], srcA);
+                const float y0 = __shfl_sync(0xffffffffu, s[kt][2], srcA);
+                const float y1 = __shfl_sync(0xffffffffu, s[kt][3], srcA);
+                const float z0 = __shfl_sync(0xffffffffu, s[kt][0], srcB);
+                const float z1 = __shfl_sync(0xffffffffu, s[kt][1], srcB);
+                const float w0 = __shfl_sync(0xffffffffu, s[kt][2], srcB);
+                const float w1 = __shfl_sync(0xffffffffu, s[kt][3], srcB);
+                pa[0] = odd ? x1 : x0;  // P[g][t]
+                pa[1] = odd ? y1 : y0;  // P[g+8][t]
+                pa[2] = odd ? z1 : z0;  // P[g][t+4]
+                pa[3] = odd ? w1 : w0;  // P[g+8][t+4]
+            }
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tf32_split(pa[i], ph[i], pl[i]);
+            // V rows t and t+4 of the k-step; rows past the context may hold
+            // stale bits (even NaN): they are read as zero
+            const int t0 = kt * 8 + tig, t1 = t0 + 4;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+                if (t0 < nvalid) v0 = lds128(vaddr + swz_offset<BS>(t0, g * 8 + gid));
+                if (t1 < nvalid) v1 = lds128(vaddr + swz_offset<BS>(t1, g * 8 + gid));
+                const float f0[4] = {__uint_as_float(v0.x), __uint_as_float(v0.y),
+                                     __uint_as_float(v0.z), __uint_as_float(v0.w)};
+                const float f1[4] = {__uint_as_float(v1.x), __uint_as_float(v1.y),
+                                     __uint_as_float(v1.z), __uint_as_float(v1.w)};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t bh0, bl0, bh1, bl1;
+                    tf32_split(f0[j], bh0, bl0);
+                    tf32_split(f1[j], bh1, bl1);
+                    mma_tf32x3(o[g][j], ph, pl, bh0, bh1, bl0, bl1);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish(WarpState<RG, D> *st, int lane) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // C columns 2t and 2t+1 of n-tile j are head columns 32g + 8t + j and +4
+                const int d0 = g * 32 + 8 * tig + j, d1 = d0 + 4;
+                st->o[gid][d0] = o[g][j][0];
+                st->o[gid][d1] = o[g][j][1];
+                if constexpr (RG == 16) {
+                    st->o[gid + 8][d0] = o[g][j][2];
+                    st->o[gid + 8][d1] = o[g][j][3];
+                }
+            }
+        if (tig == 0) {
+            // a warp that saw no block has no reference: it must not set M
+            st->m[gid] = fresh ? -CUDART_INF_F : m0;
+            st->l[gid] = l0;
+            if constexpr (RG == 16) {
+                st->m[gid + 8] = fresh ? -CUDART_INF_F : m1;
+                st->l[gid + 8] = l1;
+            }
+        }
+    }
+};
+
 // ------------------------------------------------------------------ kernel
 
 template <typename T, int D, int BS, int GP, bool MMA>
@@ -493,6 +732,10 @@ struct PathOf<__nv_bfloat16, D, BS, GP, true> {
 template <int D, int BS, int GP>
 struct PathOf<__half, D, BS, GP, true> {
     using type = MmaPath<__half, D, BS, GP>;
+};
+template <int D, int BS, int GP>
+struct PathOf<float, D, BS, GP, true> {
+    using type = Tf32Path<D, BS, GP>;
 };
 
 template <typename T, int D, int BS, int GP, bool MMA, bool RUNS>
@@ -689,7 +932,7 @@ pkv_status launch_one(const DecodeLaunch &L) {
 
 template <typename T, int D, int BS, bool RUNS>
 pkv_status launch_bs(const DecodeLaunch &L) {
-    if constexpr (sizeof(T) == 2) {
+    if constexpr (sizeof(T) == 2 || D <= 128) {
         if (L.mma)
             return L.group_pad <= 8 ? launch_one<T, D, BS, 8, true, RUNS>(L)
                                     : launch_one<T, D, BS, 16, true, RUNS>(L);

@@ -20,6 +20,9 @@ constexpr int kMaxGroup = 16;
 // of every row's query and accumulator, and 16 rows spilled (fp32, G = 16:
 // 0.14 of the copy peak whole, 0.38 in CTAs of 8 rows, 0.40 in CTAs of 4)
 constexpr int kFmaRowsMax = 4;
+// fp32 storage: groups from this size on take TF32 tensor-core tiles (a
+// 16-row tile costs the same for any group; CUDA cores win up to 4 rows)
+constexpr int kTf32MinGroup = 5;
 constexpr int kMaxStageRows = 16;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 // Query rows of a shared-prefix work item for a head size: two 16-row tiles

@@ -122,7 +122,8 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert _decode(lib, pool, flags=9) == E
     assert _decode(lib, pool, scale=float("nan")) == E
     assert _decode(lib, pool, max_blocks=0) == E
-    assert _decode(lib, _fake_pool(dtype=pagedkv.F32), flags=pagedkv.PATH_MMA) == U
+    # fp32 tensor-core tiles (TF32) are built up to head size 128
+    assert _decode(lib, _fake_pool(dtype=pagedkv.F32, head_dim=256), flags=pagedkv.PATH_MMA) == U
     assert _decode(lib, pool, num_seqs=0) == pagedkv.OK              # nothing to do
 
 

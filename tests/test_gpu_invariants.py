@@ -93,7 +93,7 @@ def test_fma_and_mma_paths_agree():
 
 
 def test_nan_in_unused_slots_is_ignored():
-    for dtype, H, Hkv in (("bf16", 32, 8), ("bf16", 8, 8), ("f32", 4, 2)):
+    for dtype, H, Hkv in (("bf16", 32, 8), ("bf16", 8, 8), ("f32", 4, 2), ("f32", 16, 2)):
         w = workload.build("nan", dtype=dtype, context_lens=[17, 5, 250, 33], num_heads=H,
                            num_kv_heads=Hkv, head_dim=128, block_size=16, data_seed=51,
                            meta_seed=52, pool_blocks=40, tail_fill=float("nan"))

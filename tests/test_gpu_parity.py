@@ -78,6 +78,9 @@ CASES = [
     ("f32", 64, 16, 12, 1),
     ("f32", 128, 16, 10, 1),
     ("bf16", 128, 16, 12, 1),
+    # fp32 groups above 4 take TF32 tensor-core tiles by default
+    ("f32", 128, 16, 12, 2),
+    ("f32", 64, 16, 8, 1),
 ]
 
 
@@ -87,7 +90,7 @@ def test_decode_matches_oracle(case, partition):
     dtype, D, BS, H, Hkv = case
     w = _w(dtype, D, BS, H, Hkv, seed=CASES.index(case))
     ref, _, _ = oracle_after_write(w)
-    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_FMA] + ([pagedkv.PATH_MMA] if dtype == "bf16" else [])
+    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_FMA, pagedkv.PATH_MMA]
     for path in paths:
         dw = run_decode(w, path=path, partition_tokens=partition)
         assert pagedkv.get_device_error(dw.pool) == 0
@@ -159,7 +162,7 @@ def test_large_blocks_match_oracle(case):
     ctx = [1, 31, 32, 33, BS - 1, BS, BS + 1, 3 * BS + 17, 1000]
     w = _w(dtype, D, BS, H, Hkv, ctx=ctx, seed=400 + LARGE_BLOCK_CASES.index(case))
     ref, _, _ = oracle_after_write(w)
-    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_FMA] + ([pagedkv.PATH_MMA] if dtype == "bf16" else [])
+    paths = [pagedkv.PATH_AUTO, pagedkv.PATH_FMA, pagedkv.PATH_MMA]
     for pt in (-1, 0, 2 * BS):
         for path in paths:
             dw = run_decode(w, path=path, partition_tokens=pt)
