@@ -307,11 +307,9 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     a.unit_shift = unit_shift;
     a.scale_log2 = scale * 1.4426950408889634f;
 
-    // the tensor-core kernels of a 256-wide head (16-bit storage) and of a
-    // 128-wide head (fp32 storage, TF32) hold ~255 registers a thread: two
-    // CTAs per SM instead of three
-    const int ctas_per_sm =
-        (mma && (pool->head_dim == 256 || (!half16 && pool->head_dim == 128))) ? 2 : 3;
+    // the tensor-core kernel of a 256-wide head holds 254 registers a thread:
+    // two CTAs per SM instead of three
+    const int ctas_per_sm = (pool->head_dim == 256 && mma) ? 2 : 3;
     const int pt = resolve_partition(partition_tokens, ctx_cap,
                                      (long long)num_seqs * num_kv_heads * a.row_split, sm_count(dev),
                                      ctas_per_sm);

@@ -96,9 +96,15 @@ constexpr int decode_ring_bytes() {
     constexpr int st = kDecodeWarps * (int)sizeof(WarpState<RG, D>);
     return ring > st ? ring : st;
 }
-template <typename T, int D, int BS, int RG>
+// bytes of the TF32 path's shared query fragments (KS k-steps x 32 lanes x 16 B)
+template <int D>
+constexpr int tf32_qbuf_bytes() {
+    return (D / 8) * 32 * 16;
+}
+template <typename T, int D, int BS, int RG, bool QBUF = false>
 constexpr int decode_smem_bytes() {
-    return decode_ring_bytes<T, D, BS, RG>() + kDecodeWarps * decode_stages<T, D, BS>() * 8 + 1024;
+    return decode_ring_bytes<T, D, BS, RG>() + kDecodeWarps * decode_stages<T, D, BS>() * 8 +
+           (QBUF ? tf32_qbuf_bytes<D>() + 16 : 0) + 1024;
 }
 
 __device__ __forceinline__ float load_as_float(const float *p) { return *p; }
@@ -529,31 +535,45 @@ struct Tf32Path {
     static constexpr int NG = D / 32;  // 32-column groups of O
     static_assert(BS == 16 && D % 32 == 0, "tile shape");
 
-    uint32_t qh[KS][4], ql[KS][4];  // A fragments of Q (rows g, g+8): high part and remainder
+    // A 128-wide head keeps the query fragments in shared memory, one fp32
+    // copy per CTA (in registers, high parts and remainders would take 128
+    // a thread and cap the kernel at two CTAs per SM); a 64-wide head keeps
+    // them in registers (measured faster: 0.78-0.82 of the copy peak against
+    // 0.74-0.75 from shared memory)
+    static constexpr bool kSharedQ = D > 64;
+    uint32_t qbuf;                              // shared fragments: [KS][lane] x 4 fp32
+    uint32_t qh[kSharedQ ? 1 : KS][4], ql[kSharedQ ? 1 : KS][4];  // register fragments
     float o[NG][4][4];              // O accumulators: column group, n-tile, C fragment
     float m0, m1, l0, l1;           // rows g and g+8: reference, lane-partial sum
     float scale_log2;
     int gid, tig;
     bool fresh;                     // no block seen yet
 
-    __device__ __forceinline__ void init(const float *qrow0, int group, float sl2, int lane) {
+    // With shared fragments the CTA's warps write one copy, each warp every
+    // nwarps-th k-step, and the caller syncs the CTA before the first block.
+    __device__ __forceinline__ void init(const float *qrow0, int group, float sl2, int lane,
+                                         uint32_t qb, int warp, int nwarps) {
         gid = lane >> 2;
         tig = lane & 3;
         scale_log2 = sl2;
         fresh = true;
         m0 = m1 = 0.f;
         l0 = l1 = 0.f;
+        qbuf = qb;
+        auto qval = [&](int ks, int i) -> float {  // fragment value i of k-step ks
+            const int r = gid + (i & 1) * 8, c = ks * 8 + tig + (i >> 1) * 4;
+            return r < group ? __ldg(qrow0 + (size_t)r * D + c) : 0.f;
+        };
+        if constexpr (kSharedQ) {
+            for (int ks = warp; ks < KS; ks += nwarps)
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(qbuf + (ks * 32 + lane) * 16),
+                             "f"(qval(ks, 0)), "f"(qval(ks, 1)), "f"(qval(ks, 2)), "f"(qval(ks, 3))
+                             : "memory");
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int c0 = ks * 8 + tig, c1 = c0 + 4;
-            const float x0 = gid < group ? __ldg(qrow0 + (size_t)gid * D + c0) : 0.f;
-            const float x1 = gid + 8 < group ? __ldg(qrow0 + (size_t)(gid + 8) * D + c0) : 0.f;
-            const float x2 = gid < group ? __ldg(qrow0 + (size_t)gid * D + c1) : 0.f;
-            const float x3 = gid + 8 < group ? __ldg(qrow0 + (size_t)(gid + 8) * D + c1) : 0.f;
-            tf32_split(x0, qh[ks][0], ql[ks][0]);
-            tf32_split(x1, qh[ks][1], ql[ks][1]);
-            tf32_split(x2, qh[ks][2], ql[ks][2]);
-            tf32_split(x3, qh[ks][3], ql[ks][3]);
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tf32_split(qval(ks, i), qh[ks][i], ql[ks][i]);
         }
 #pragma unroll
         for (int g = 0; g < NG; ++g)
@@ -570,6 +590,20 @@ struct Tf32Path {
         const int ktok = (lane >> 4) * 8 + (lane & 7);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
+            uint32_t ah[4], al[4];
+            if constexpr (kSharedQ) {
+                const uint4 qv = lds128(qbuf + (ks * 32 + lane) * 16);
+                tf32_split(__uint_as_float(qv.x), ah[0], al[0]);
+                tf32_split(__uint_as_float(qv.y), ah[1], al[1]);
+                tf32_split(__uint_as_float(qv.z), ah[2], al[2]);
+                tf32_split(__uint_as_float(qv.w), ah[3], al[3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ah[i] = qh[ks][i];
+                    al[i] = ql[ks][i];
+                }
+            }
             uint32_t r[4];
             ldsm_x4(kaddr + swz_offset<BS>(ktok, ks * 2 + ((lane >> 3) & 1)), r[0], r[1], r[2], r[3]);
             uint32_t kh[4], kl[4];
@@ -577,7 +611,7 @@ struct Tf32Path {
             for (int i = 0; i < 4; ++i) tf32_split(__uint_as_float(r[i]), kh[i], kl[i]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                mma_tf32x3(s[nt], qh[ks], ql[ks], kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
+                mma_tf32x3(s[nt], ah, al, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
         }
         // online softmax against a lazy reference (as on the 16-bit path)
         if (nvalid < BS) {
@@ -748,6 +782,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     constexpr int NST = decode_stages<T, D, BS>();
     constexpr int RG = GP;  // rows of the exported warp state
     constexpr int RING = decode_ring_bytes<T, D, BS, RG>();
+    constexpr bool TF32 = MMA && sizeof(T) == 4;  // fp32 storage on tensor cores
+    constexpr bool QBUF = TF32 && D > 64;          // with the query fragments in shared memory
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -834,7 +870,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     Path path;
     const T *qrow0 = reinterpret_cast<const T *>(a.q) +
                      ((size_t)s * a.num_heads + (size_t)g * a.group + r0) * D;
-    path.init(qrow0, nrows, a.scale_log2, lane);
+    if constexpr (TF32) {
+        // (the shared fragments sit after the barriers: the ring is reused
+        // for the warps' states)
+        constexpr int qoff = (RING + NW * NST * 8 + 15) & ~15;
+        path.init(qrow0, nrows, a.scale_log2, lane, smem_u32(smem + qoff), warp, NW);
+        if constexpr (QBUF) __syncthreads();  // every warp's share of the fragments is written
+    } else {
+        path.init(qrow0, nrows, a.scale_log2, lane);
+    }
 
 #pragma unroll 1
     for (int i = 0; i < NST && i < nw; ++i) issue(i, bt_get(i));
@@ -914,7 +958,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 template <typename T, int D, int BS, int GP, bool MMA, bool RUNS>
 pkv_status launch_one(const DecodeLaunch &L) {
     auto kern = paged_decode_kernel<T, D, BS, GP, MMA, RUNS>;
-    constexpr int smem = decode_smem_bytes<T, D, BS, GP>();
+    constexpr int smem = decode_smem_bytes<T, D, BS, GP, MMA && sizeof(T) == 4 && (D > 64)>();
     static_assert(smem <= 227 * 1024, "shared memory budget");
     // Raise the dynamic shared-memory limit once per device for this kernel.
     static unsigned long long done_mask = 0ull;
