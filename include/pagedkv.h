@@ -71,7 +71,9 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
 #define PKV_DECODE_PATH_AUTO 0  /* tensor cores when the GQA group makes dense tiles */
 #define PKV_DECODE_PATH_FMA 1   /* CUDA-core dot products for every group size (groups above
                                    4 rows are split over CTAs of the same kv head) */
-#define PKV_DECODE_PATH_MMA 2   /* tensor-core tiles (bf16 or fp16 pools) for every group size */
+#define PKV_DECODE_PATH_MMA 2   /* tensor-core tiles for every group size: bf16/fp16 tiles for
+                                   16-bit pools, TF32 tiles with three products each for fp32
+                                   pools (head_dim 64 or 128) */
 
 /*
  * Block pool: K and V are separate device buffers, each laid out
@@ -166,9 +168,10 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
  *
  * query: device [num_seqs][num_heads][head_dim] in the pool dtype.
  * out: device [num_seqs][num_heads][head_dim] in out_dtype (F32, BF16 or
- *   F16).  Scores and sums are fp32 whatever the storage type; tensor-core
- *   tiles (PKV_DECODE_PATH_MMA, and AUTO for groups of 4 or more) take BF16
- *   or F16 pools.
+ *   F16).  Scores and sums are fp32 whatever the storage type.  AUTO takes
+ *   tensor-core tiles for groups of 4 or more with BF16 or F16 pools and for
+ *   groups of 5 or more with F32 pools (TF32, each product as three TF32
+ *   products, within the fp32 tolerance), CUDA-core dot products otherwise.
  * block_tables: device int32 [num_seqs][max_blocks_per_seq].
  * context_lens: device int32 [num_seqs].
  * max_context_len: host upper bound on every context length (grid sizing;
