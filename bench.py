@@ -265,10 +265,10 @@ def workload_config(w, name: str, world: int, overrides: dict | None = None) -> 
 
 
 def shared_prefix_supported(w) -> bool:
-    """Shapes the shared-prefix decode takes (16-bit pools, blocks that are
-    whole 16-row runs, groups up to 16)."""
-    return (w.dtype in ("bf16", "f16") and w.block_size % 16 == 0
-            and w.num_heads // w.num_kv_heads <= 16)
+    """Shapes the shared-prefix decode takes (16-bit pools, or fp32 pools up
+    to head size 128; blocks that are whole 16-row runs; groups up to 16)."""
+    return ((w.dtype in ("bf16", "f16") or (w.dtype == "f32" and w.head_dim <= 128))
+            and w.block_size % 16 == 0 and w.num_heads // w.num_kv_heads <= 16)
 
 
 def time_launches(fn, stream, min_seconds: float, warmup: int = 3,

@@ -169,9 +169,11 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
  * query: device [num_seqs][num_heads][head_dim] in the pool dtype.
  * out: device [num_seqs][num_heads][head_dim] in out_dtype (F32, BF16 or
  *   F16).  Scores and sums are fp32 whatever the storage type.  AUTO takes
- *   tensor-core tiles for groups of 4 or more with BF16 or F16 pools and for
- *   groups of 5 or more with F32 pools (TF32, each product as three TF32
- *   products, within the fp32 tolerance), CUDA-core dot products otherwise.
+ *   tensor-core tiles for groups of 4 or more with BF16 or F16 pools and,
+ *   with F32 pools, for groups of 9 or more at head_dim 128 and of 5 or more
+ *   at head_dim 64 (TF32, each product as three TF32 products, each k-step
+ *   summed in fp32: within the fp32 tolerance), CUDA-core dot products
+ *   otherwise.
  * block_tables: device int32 [num_seqs][max_blocks_per_seq].
  * context_lens: device int32 [num_seqs].
  * max_context_len: host upper bound on every context length (grid sizing;
@@ -292,8 +294,9 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: BF16 or F16
  * pools (head_dim 64, 128 or 256; the work items of 64- and 256-wide heads
- * carry 16 query rows instead of 32), num_heads / num_kv_heads in 1..16, out_dtype
- * F32, BF16 or F16.
+ * carry 16 query rows instead of 32), and F32 pools of head_dim 64 or 128
+ * (items of 16 rows as TF32 tiles, three products each, k-steps summed in
+ * fp32), num_heads / num_kv_heads in 1..16, out_dtype F32, BF16 or F16.
  */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_context_len, int max_prefix_len,

@@ -266,7 +266,7 @@ static pkv_status decode_impl(const pkv_pool *pool, bool contig, void *out, pkv_
     if (num_kv_heads > 65535 || num_seqs > 65535) return PKV_ERR_UNSUPPORTED;  // grid y
     const bool half16 = pool->dtype != PKV_F32;  // bf16 or fp16: 16-bit tensor-core tiles
     // fp32 storage takes TF32 tiles (three products each) for the larger groups
-    bool mma = half16 ? group >= 4 : group >= kTf32MinGroup;
+    bool mma = half16 ? group >= 4 : group >= tf32_min_group(pool->head_dim);
     if (flags == PKV_DECODE_PATH_FMA) mma = false;
     if (flags == PKV_DECODE_PATH_MMA) {
         if (!half16 && pool->head_dim > 128) return PKV_ERR_UNSUPPORTED;

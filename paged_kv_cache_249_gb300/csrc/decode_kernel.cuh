@@ -510,8 +510,12 @@ __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// a*b to about fp32 accuracy from three TF32 products: hi*hi + hi*lo + lo*hi
-// (the lo*lo term is below 2^-22 of the product)
+// a*b from three TF32 products, hi*hi + hi*lo + lo*hi (the lo*lo term is
+// below 2^-22 of the product).  Callers start each chain from a zero
+// accumulator and add it to their running sums with rounded fp32 adds: the
+// tensor cores' own accumulation onto a large running sum loses low bits
+// with a bias (on scores of ~100 in log2 units the error grew 5x above the
+// CUDA-core fp32 path's; with zero-started chains it matches it)
 __device__ __forceinline__ void mma_tf32x3(float (&d)[4], const uint32_t (&ah)[4],
                                            const uint32_t (&al)[4], uint32_t bh0, uint32_t bh1,
                                            uint32_t bl0, uint32_t bl1) {
@@ -520,9 +524,11 @@ __device__ __forceinline__ void mma_tf32x3(float (&d)[4], const uint32_t (&ah)[4
     mma_tf32_1688(d, ah, bh0, bh1);
 }
 
+
 // fp32 storage on tensor cores: the G query rows (padded to 16) as m16n8k8
-// TF32 tiles, each product taken as three TF32 products so that scores and
-// outputs keep about fp32 accuracy.  K fragments come from the swizzled
+// TF32 tiles, each product as three TF32 products, each k-step (and each
+// block's P V) from a zero accumulator added by rounded fp32 adds, so that
+// scores and outputs keep about fp32 accuracy.  K fragments come from the swizzled
 // stage with ldmatrix (an 8-row, 16-byte matrix of the 16-bit view holds an
 // 8x4 block of fp32, one value per lane, which is what a TF32 B fragment
 // wants); V fragments with 16-byte loads, four O columns at a time, so O's
@@ -535,21 +541,17 @@ struct Tf32Path {
     static constexpr int NG = D / 32;  // 32-column groups of O
     static_assert(BS == 16 && D % 32 == 0, "tile shape");
 
-    // A 128-wide head keeps the query fragments in shared memory, one fp32
-    // copy per CTA (in registers, high parts and remainders would take 128
-    // a thread and cap the kernel at two CTAs per SM); a 64-wide head keeps
-    // them in registers (measured faster: 0.78-0.82 of the copy peak against
-    // 0.74-0.75 from shared memory)
-    static constexpr bool kSharedQ = D > 64;
-    uint32_t qbuf;                              // shared fragments: [KS][lane] x 4 fp32
-    uint32_t qh[kSharedQ ? 1 : KS][4], ql[kSharedQ ? 1 : KS][4];  // register fragments
+    // The query fragments sit in shared memory, one fp32 copy per CTA, and
+    // are split per k-step (three TF32 parts a value would take 3 * D / 2
+    // registers a thread).
+    uint32_t qbuf;                  // shared fragments: [KS][lane] x 4 fp32
     float o[NG][4][4];              // O accumulators: column group, n-tile, C fragment
     float m0, m1, l0, l1;           // rows g and g+8: reference, lane-partial sum
     float scale_log2;
     int gid, tig;
     bool fresh;                     // no block seen yet
 
-    // With shared fragments the CTA's warps write one copy, each warp every
+    // The CTA's warps write one copy of the fragments, each warp every
     // nwarps-th k-step, and the caller syncs the CTA before the first block.
     __device__ __forceinline__ void init(const float *qrow0, int group, float sl2, int lane,
                                          uint32_t qb, int warp, int nwarps) {
@@ -564,17 +566,10 @@ struct Tf32Path {
             const int r = gid + (i & 1) * 8, c = ks * 8 + tig + (i >> 1) * 4;
             return r < group ? __ldg(qrow0 + (size_t)r * D + c) : 0.f;
         };
-        if constexpr (kSharedQ) {
-            for (int ks = warp; ks < KS; ks += nwarps)
-                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(qbuf + (ks * 32 + lane) * 16),
-                             "f"(qval(ks, 0)), "f"(qval(ks, 1)), "f"(qval(ks, 2)), "f"(qval(ks, 3))
-                             : "memory");
-        } else {
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) tf32_split(qval(ks, i), qh[ks][i], ql[ks][i]);
-        }
+        for (int ks = warp; ks < KS; ks += nwarps)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(qbuf + (ks * 32 + lane) * 16),
+                         "f"(qval(ks, 0)), "f"(qval(ks, 1)), "f"(qval(ks, 2)), "f"(qval(ks, 3))
+                         : "memory");
 #pragma unroll
         for (int g = 0; g < NG; ++g)
 #pragma unroll
@@ -590,28 +585,27 @@ struct Tf32Path {
         const int ktok = (lane >> 4) * 8 + (lane & 7);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
+            const uint4 qv = lds128(qbuf + (ks * 32 + lane) * 16);
+            const float qf[4] = {__uint_as_float(qv.x), __uint_as_float(qv.y), __uint_as_float(qv.z),
+                                 __uint_as_float(qv.w)};
             uint32_t ah[4], al[4];
-            if constexpr (kSharedQ) {
-                const uint4 qv = lds128(qbuf + (ks * 32 + lane) * 16);
-                tf32_split(__uint_as_float(qv.x), ah[0], al[0]);
-                tf32_split(__uint_as_float(qv.y), ah[1], al[1]);
-                tf32_split(__uint_as_float(qv.z), ah[2], al[2]);
-                tf32_split(__uint_as_float(qv.w), ah[3], al[3]);
-            } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    ah[i] = qh[ks][i];
-                    al[i] = ql[ks][i];
-                }
-            }
+            for (int i = 0; i < 4; ++i) tf32_split(qf[i], ah[i], al[i]);
             uint32_t r[4];
             ldsm_x4(kaddr + swz_offset<BS>(ktok, ks * 2 + ((lane >> 3) & 1)), r[0], r[1], r[2], r[3]);
             uint32_t kh[4], kl[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) tf32_split(__uint_as_float(r[i]), kh[i], kl[i]);
+            // each k-step from a zero accumulator, added to the scores by a
+            // rounded fp32 add (the tensor cores' own accumulation, on a large
+            // running sum, loses low bits with a bias)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma_tf32x3(s[nt], ah, al, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
+            for (int nt = 0; nt < NT; ++nt) {
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_tf32x3(t, ah, al, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += t[e];
+            }
         }
         // online softmax against a lazy reference (as on the 16-bit path)
         if (nvalid < BS) {
@@ -680,6 +674,7 @@ struct Tf32Path {
         // t+4) by shuffles inside each group of four lanes.
         const int base = lane & ~3, srcA = base + (tig >> 1), srcB = srcA + 2;
         const bool odd = tig & 1;
+        uint32_t ph[NT][4], pl[NT][4];
 #pragma unroll
         for (int kt = 0; kt < NT; ++kt) {
             float pa[4];
@@ -697,28 +692,39 @@ struct Tf32Path {
                 pa[2] = odd ? z1 : z0;  // P[g][t+4]
                 pa[3] = odd ? w1 : w0;  // P[g+8][t+4]
             }
-            uint32_t ph[4], pl[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tf32_split(pa[i], ph[i], pl[i]);
-            // V rows t and t+4 of the k-step; rows past the context may hold
-            // stale bits (even NaN): they are read as zero
-            const int t0 = kt * 8 + tig, t1 = t0 + 4;
+            for (int i = 0; i < 4; ++i) tf32_split(pa[i], ph[kt][i], pl[kt][i]);
+        }
+        // this block's P V from zero accumulators, added to O by rounded fp32
+        // adds.  V rows past the context may hold stale bits (even NaN): they
+        // are read as zero
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-                if (t0 < nvalid) v0 = lds128(vaddr + swz_offset<BS>(t0, g * 8 + gid));
-                if (t1 < nvalid) v1 = lds128(vaddr + swz_offset<BS>(t1, g * 8 + gid));
-                const float f0[4] = {__uint_as_float(v0.x), __uint_as_float(v0.y),
-                                     __uint_as_float(v0.z), __uint_as_float(v0.w)};
-                const float f1[4] = {__uint_as_float(v1.x), __uint_as_float(v1.y),
-                                     __uint_as_float(v1.z), __uint_as_float(v1.w)};
+        for (int g = 0; g < NG; ++g) {
+            float f[NT][2][4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t bh0, bl0, bh1, bl1;
-                    tf32_split(f0[j], bh0, bl0);
-                    tf32_split(f1[j], bh1, bl1);
-                    mma_tf32x3(o[g][j], ph, pl, bh0, bh1, bl0, bl1);
+            for (int kt = 0; kt < NT; ++kt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = kt * 8 + tig + 4 * h;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (t < nvalid) v = lds128(vaddr + swz_offset<BS>(t, g * 8 + gid));
+                    f[kt][h][0] = __uint_as_float(v.x);
+                    f[kt][h][1] = __uint_as_float(v.y);
+                    f[kt][h][2] = __uint_as_float(v.z);
+                    f[kt][h][3] = __uint_as_float(v.w);
                 }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kt = 0; kt < NT; ++kt) {
+                    uint32_t bh0, bl0, bh1, bl1;
+                    tf32_split(f[kt][0][j], bh0, bl0);
+                    tf32_split(f[kt][1][j], bh1, bl1);
+                    mma_tf32x3(t, ph[kt], pl[kt], bh0, bh1, bl0, bl1);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[g][j][e] += t[e];
             }
         }
     }
@@ -783,7 +789,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     constexpr int RG = GP;  // rows of the exported warp state
     constexpr int RING = decode_ring_bytes<T, D, BS, RG>();
     constexpr bool TF32 = MMA && sizeof(T) == 4;  // fp32 storage on tensor cores
-    constexpr bool QBUF = TF32 && D > 64;          // with the query fragments in shared memory
+    constexpr bool QBUF = TF32;                    // with the query fragments in shared memory
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -958,7 +964,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 template <typename T, int D, int BS, int GP, bool MMA, bool RUNS>
 pkv_status launch_one(const DecodeLaunch &L) {
     auto kern = paged_decode_kernel<T, D, BS, GP, MMA, RUNS>;
-    constexpr int smem = decode_smem_bytes<T, D, BS, GP, MMA && sizeof(T) == 4 && (D > 64)>();
+    constexpr int smem = decode_smem_bytes<T, D, BS, GP, MMA && sizeof(T) == 4>();
     static_assert(smem <= 227 * 1024, "shared memory budget");
     // Raise the dynamic shared-memory limit once per device for this kernel.
     static unsigned long long done_mask = 0ull;

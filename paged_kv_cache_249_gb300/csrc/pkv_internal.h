@@ -21,8 +21,11 @@ constexpr int kMaxGroup = 16;
 // 0.14 of the copy peak whole, 0.38 in CTAs of 8 rows, 0.40 in CTAs of 4)
 constexpr int kFmaRowsMax = 4;
 // fp32 storage: groups from this size on take TF32 tensor-core tiles (a
-// 16-row tile costs the same for any group; CUDA cores win up to 4 rows)
-constexpr int kTf32MinGroup = 5;
+// 16-row tile costs the same for any group).  Measured on the gqa_8b batch
+// (decode µs, CUDA cores / TF32): head 128, G = 5, 8, 12, 16: 945 / 976,
+// 952 / 986, 1338 / 1036, 1736 / 1046; head 64, G = 5, 16: 644 / 496,
+// 1250 / 527.
+constexpr int tf32_min_group(int head_dim) { return head_dim == 128 ? 9 : 5; }
 constexpr int kMaxStageRows = 16;  // rows of one staged run; larger blocks are staged in runs
 constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work item (two MMA tiles)
 // Query rows of a shared-prefix work item for a head size: two 16-row tiles
@@ -30,7 +33,10 @@ constexpr int kSpRowsMax = 32;  // shared-prefix decode: query rows per work ite
 // registers) and for a 64-wide one, whose lighter items then fit four CTAs
 // per SM (measured faster than two CTAs of two-tile items, although a group
 // with more members than one item holds reads its prefix once per item).
-constexpr int sp_rows_for(int head_dim) { return head_dim == 128 ? kSpRowsMax : 16; }
+// fp32 storage takes one tile at every head size (fp32 accumulators of TF32 tiles).
+constexpr int sp_rows_for(int head_dim, int elem_bytes = 2) {
+    return head_dim == 128 && elem_bytes == 2 ? kSpRowsMax : 16;
+}
 
 // Arguments of one decode launch; every pointer is a device pointer.
 struct DecodeArgs {
@@ -143,6 +149,8 @@ pkv_status launch_shared_prefix_f16_d64(const SpLaunch &L);
 pkv_status launch_shared_prefix_f16_d128(const SpLaunch &L);
 pkv_status launch_shared_prefix_d256(const SpLaunch &L);      // bf16 pools
 pkv_status launch_shared_prefix_f16_d256(const SpLaunch &L);
+pkv_status launch_shared_prefix_f32_d64(const SpLaunch &L);
+pkv_status launch_shared_prefix_f32_d128(const SpLaunch &L);
 
 pkv_status launch_decode_f32_d64(const DecodeLaunch &L);
 pkv_status launch_decode_f32_d128(const DecodeLaunch &L);

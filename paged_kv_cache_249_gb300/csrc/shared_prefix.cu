@@ -430,8 +430,9 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
         (partition_tokens > 0 && partition_tokens % c.BS != 0))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    // tensor-core tiles of bf16 or fp16 (fp32 pools take the plain decode)
-    if (pool->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;
+    // tensor-core tiles: bf16 or fp16, or TF32 (three products each) for fp32
+    // pools of head size 64 or 128
+    if (pool->dtype == PKV_F32 && pool->head_dim > 128) return PKV_ERR_UNSUPPORTED;
     // blocks above kMaxStageRows tokens are staged (and listed) in runs
     c.U = c.BS < kMaxStageRows ? c.BS : kMaxStageRows;
     if (c.U != kMaxStageRows) return PKV_ERR_UNSUPPORTED;  // blocks are whole 16-row runs
@@ -480,7 +481,7 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
     p.pbp = c.z.ptp > 0 ? c.z.ptp / c.U
                         : ((c.maxp + c.U - 1) / c.U > 0 ? (c.maxp + c.U - 1) / c.U : 1);
     p.pbs = c.z.pts > 0 ? c.z.pts / c.U : (c.cap_blocks > 0 ? c.cap_blocks : 1);
-    p.members_per_item = sp_rows_for(pool->head_dim) / c.group;
+    p.members_per_item = sp_rows_for(pool->head_dim, pool->dtype == PKV_F32 ? 4 : 2) / c.group;
     // least shift with (cap - 1) >> shift < kPlanClasses
     auto cls_shift = [](int cap) {
         int sh = 0;
@@ -545,7 +546,9 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     L.device = c.dev;
     const int hd = pool->head_dim;
     const pkv_status s1 =
-        pool->dtype == PKV_F16
+        pool->dtype == PKV_F32
+            ? (hd == 64 ? launch_shared_prefix_f32_d64(L) : launch_shared_prefix_f32_d128(L))
+        : pool->dtype == PKV_F16
             ? (hd == 64 ? launch_shared_prefix_f16_d64(L)
                         : (hd == 128 ? launch_shared_prefix_f16_d128(L) : launch_shared_prefix_f16_d256(L)))
             : (hd == 64 ? launch_shared_prefix_d64(L)

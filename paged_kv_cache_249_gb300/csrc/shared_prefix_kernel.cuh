@@ -26,16 +26,18 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "decode_kernel.cuh"
 
 namespace pkv {
 
 constexpr int kSpWarps = 4;
 // query rows and 16-row accumulator tiles of one item
-template <int D>
-constexpr int kSpRows = sp_rows_for(D);
-template <int D>
-constexpr int kSpTiles = kSpRows<D> / 16;
+template <typename T, int D>
+constexpr int kSpRows = sp_rows_for(D, (int)sizeof(T));
+template <typename T, int D>
+constexpr int kSpTiles = kSpRows<T, D> / 16;
 // Shared memory per CTA: two CTAs (8 warps) per SM for 128- and 256-wide
 // heads, which is what the register budget of their accumulators allows, and
 // four CTAs (16 warps) for the one-tile items of a 64-wide head.  Each warp's
@@ -45,10 +47,10 @@ constexpr int kSpTiles = kSpRows<D> / 16;
 template <int D>
 constexpr int kSpSmemTarget = D == 64 ? 55 * 1024 : 112 * 1024;
 
-template <int D, int BS>
+template <typename T, int D, int BS>
 struct SpSmem {
-    using Gm = Geom<__nv_bfloat16, D, BS>;  // sizes only: the same for fp16
-    static constexpr int kQ = kSpRows<D> * D * 2;  // a warp's query rows (16-bit, swizzled slabs)
+    using Gm = Geom<T, D, BS>;
+    static constexpr int kQ = kSpRows<T, D> * D * (int)sizeof(T);  // a warp's query rows (swizzled slabs)
     static constexpr int kMisc = 256;
     static constexpr int kFixed = kSpWarps * kQ + kMisc + 1024;
     static constexpr int kStagesFit = (kSpSmemTarget<D> - kFixed) / (kSpWarps * Gm::kStageBytes);
@@ -92,7 +94,7 @@ template <typename T, int D, int BS>
 struct SpMma {
     using MM = Mma16<T>;
     static constexpr int ND = D / 8;  // n-tiles of O
-    static constexpr int NT = kSpTiles<D>;
+    static constexpr int NT = kSpTiles<T, D>;
     float o[NT][ND][4];
     // [tile][row gid / gid+8]: m is the row's reference (log2 units), l its
     // lane-partial sum of weights relative to m
@@ -310,6 +312,221 @@ struct SpMma {
     }
 };
 
+// fp32 storage: one 16-row tile of query rows as m16n8k8 TF32 tiles, each
+// product as three TF32 products, each k-step (and each block's P V) from a
+// zero accumulator added by rounded fp32 adds, so that scores and outputs
+// keep about fp32 accuracy.  Q
+// and K fragments come from their swizzled buffers by ldmatrix (an 8-row,
+// 16-byte matrix of the 16-bit view is an 8x4 block of fp32, one value a
+// lane); P moves from the accumulator layout to the A layout by shuffles in
+// each group of four lanes; V fragments come by 16-byte loads, four O
+// columns at a time, so that inside each 32-column group column 32g + 4n + j
+// is n-tile j's column n.  The online softmax keeps the lazy reference of
+// the 16-bit tiles.
+template <int D, int BS>
+struct SpTf32 {
+    static constexpr int KS = D / 8;   // k-steps of the QK^T product
+    static constexpr int NG = D / 32;  // 32-column groups of O
+    float o[NG][4][4];                 // column group, n-tile, C fragment
+    float m[1][2], l[1][2];            // rows gid / gid+8: reference, lane-partial sum
+    int gid, tig;
+    bool fresh;                        // no block seen yet in this item
+
+    __device__ __forceinline__ void reset(int lane) {
+        gid = lane >> 2;
+        tig = lane & 3;
+        fresh = true;
+        m[0][0] = m[0][1] = 0.f;
+        l[0][0] = l[0][1] = 0.f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[g][j][0] = o[g][j][1] = o[g][j][2] = o[g][j][3] = 0.f;
+    }
+
+    // V rows r0+nvalid .. r0+15 of a partial run may hold stale bits (even
+    // NaN): zero them in the stage before P V reads it, fenced against the
+    // TMA refill of the slot.
+    __device__ __forceinline__ void zero_tail(uint32_t vaddr, int r0, int nvalid, int lane) {
+        constexpr int CH = D * 4 / 16;
+        for (int q = lane; q < (16 - nvalid) * CH; q += 32)
+            sts_zero16(vaddr + swz_offset<BS>(r0 + nvalid + q / CH, q % CH));
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // S = Q K^T for tokens r0 .. r0+15 (the first nvalid are context tokens)
+    // and the online softmax; P for the two 8-token k-steps of P V, as a
+    // TF32 high part and remainder in the A layout, goes to ph / pl.
+    template <int QR>
+    __device__ __forceinline__ void scores(uint32_t kaddr, uint32_t qaddr, int r0, int nvalid,
+                                           float scale_log2, int lane, uint32_t (&ph)[2][4],
+                                           uint32_t (&pl)[2][4]) {
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        // ldmatrix.x4: lane L names row (L & 7) of matrix L >> 3; for Q the
+        // matrices are (rows 0-7 | 8-15) x (columns 8ks..+3 | +4..+7), in the
+        // order of the A fragment; for K (tokens 0-7 | 8-15) x the same columns
+        const int qrow = ((lane >> 3) & 1) * 8 + (lane & 7), qhalf = lane >> 4;
+        const int ktok = r0 + (lane >> 4) * 8 + (lane & 7), khalf = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t q[4], kr[4];
+            ldsm_x4(qaddr + swz_offset<QR>(qrow, ks * 2 + qhalf), q[0], q[1], q[2], q[3]);
+            ldsm_x4(kaddr + swz_offset<BS>(ktok, ks * 2 + khalf), kr[0], kr[1], kr[2], kr[3]);
+            uint32_t ah[4], al[4], kh[4], kl[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                tf32_split(__uint_as_float(q[i]), ah[i], al[i]);
+                tf32_split(__uint_as_float(kr[i]), kh[i], kl[i]);
+            }
+            // each k-step from a zero accumulator, added by a rounded fp32 add
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_tf32x3(t, ah, al, kh[2 * nt], kh[2 * nt + 1], kl[2 * nt], kl[2 * nt + 1]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += t[e];
+            }
+        }
+        if (nvalid < 16) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    if (nt * 8 + 2 * tig + e >= nvalid) s[nt][e] = s[nt][2 + e] = -CUDART_INF_F;
+        }
+        bool grow = fresh;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                s[nt][e] = fmaf(s[nt][e], scale_log2, -m[0][0]);
+                s[nt][2 + e] = fmaf(s[nt][2 + e], scale_log2, -m[0][1]);
+                grow |= s[nt][e] > 8.f;
+                grow |= s[nt][2 + e] > 8.f;
+            }
+        if (__any_sync(0xffffffffu, grow)) {
+            float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mx0 = fmaxf(mx0, s[nt][e]);
+                    mx1 = fmaxf(mx1, s[nt][2 + e]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            // every row has a context token (nvalid >= 1), so mx is finite
+            const float d0 = fresh ? mx0 : fmaxf(mx0, 0.f), d1 = fresh ? mx1 : fmaxf(mx1, 0.f);
+            const float a0 = fresh ? 0.f : fast_exp2(-d0), a1 = fresh ? 0.f : fast_exp2(-d1);
+            m[0][0] += d0;
+            m[0][1] += d1;
+            l[0][0] *= a0;
+            l[0][1] *= a1;
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    o[g][j][0] *= a0;
+                    o[g][j][1] *= a0;
+                    o[g][j][2] *= a1;
+                    o[g][j][3] *= a1;
+                }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    s[nt][e] -= d0;
+                    s[nt][2 + e] -= d1;
+                }
+            fresh = false;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[nt][e] = fast_exp2(s[nt][e]);
+                l[0][e >> 1] += s[nt][e];
+            }
+        // C layout (row g, columns 2t, 2t+1) -> A layout (row g, columns t, t+4)
+        const int base = lane & ~3, srcA = base + (tig >> 1), srcB = srcA + 2;
+        const bool odd = tig & 1;
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+            const float x0 = __shfl_sync(0xffffffffu, s[kt][0], srcA);
+            const float x1 = __shfl_sync(0xffffffffu, s[kt][1], srcA);
+            const float y0 = __shfl_sync(0xffffffffu, s[kt][2], srcA);
+            const float y1 = __shfl_sync(0xffffffffu, s[kt][3], srcA);
+            const float z0 = __shfl_sync(0xffffffffu, s[kt][0], srcB);
+            const float z1 = __shfl_sync(0xffffffffu, s[kt][1], srcB);
+            const float w0 = __shfl_sync(0xffffffffu, s[kt][2], srcB);
+            const float w1 = __shfl_sync(0xffffffffu, s[kt][3], srcB);
+            tf32_split(odd ? x1 : x0, ph[kt][0], pl[kt][0]);  // P[g][t]
+            tf32_split(odd ? y1 : y0, ph[kt][1], pl[kt][1]);  // P[g+8][t]
+            tf32_split(odd ? z1 : z0, ph[kt][2], pl[kt][2]);  // P[g][t+4]
+            tf32_split(odd ? w1 : w0, ph[kt][3], pl[kt][3]);  // P[g+8][t+4]
+        }
+    }
+
+    // O += P V for the same tokens of the staged V block (rows past the
+    // context zeroed first).
+    __device__ __forceinline__ void accumulate(uint32_t vaddr, int r0, int lane,
+                                               const uint32_t (&ph)[2][4], const uint32_t (&pl)[2][4]) {
+        // from zero accumulators, added to O by rounded fp32 adds
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            float f[2][2][4];
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 v = lds128(vaddr + swz_offset<BS>(r0 + kt * 8 + tig + 4 * h, g * 8 + gid));
+                    f[kt][h][0] = __uint_as_float(v.x);
+                    f[kt][h][1] = __uint_as_float(v.y);
+                    f[kt][h][2] = __uint_as_float(v.z);
+                    f[kt][h][3] = __uint_as_float(v.w);
+                }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    uint32_t bh0, bl0, bh1, bl1;
+                    tf32_split(f[kt][0][j], bh0, bl0);
+                    tf32_split(f[kt][1][j], bh1, bl1);
+                    mma_tf32x3(t, ph[kt], pl[kt], bh0, bh1, bl0, bl1);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[g][j][e] += t[e];
+            }
+        }
+    }
+
+    // a block staged whole; the stale V rows are zeroed first
+    template <int MT, int QR>
+    __device__ __forceinline__ void block(uint32_t kaddr, uint32_t vaddr, uint32_t qaddr, int nvalid,
+                                          float scale_log2, int lane) {
+#pragma unroll
+        for (int h = 0; h < BS / 16; ++h) {
+            const int nv = nvalid - h * 16;
+            if (nv > 0) {
+                const int n = nv < 16 ? nv : 16;
+                if (n < 16) zero_tail(vaddr, h * 16, n, lane);
+                uint32_t ph[2][4], pl[2][4];
+                scores<QR>(kaddr, qaddr, h * 16, n, scale_log2, lane, ph, pl);
+                accumulate(vaddr, h * 16, lane, ph, pl);
+            }
+        }
+    }
+
+    // head column of C element e (0, 1) of n-tile j in column group g
+    __device__ __forceinline__ int col(int g, int j, int e) const { return g * 32 + 8 * tig + j + 4 * e; }
+};
+
 // ------------------------------------------------------------------ kernel
 
 template <typename T, int D, int BS>
@@ -317,9 +534,9 @@ __global__ void __launch_bounds__(kSpWarps * 32)
     shared_prefix_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                 const __grid_constant__ CUtensorMap tmv, const SpArgs a) {
     using Gm = Geom<T, D, BS>;
-    using Sm = SpSmem<D, BS>;
+    using Sm = SpSmem<T, D, BS>;
     constexpr int NST = Sm::NST;
-    constexpr int QCH = D * 2 / 16;  // 16-byte chunks per query row
+    constexpr int QCH = D * (int)sizeof(T) / 16;  // 16-byte chunks per query row
     constexpr int ND = D / 8;
     constexpr unsigned FULL = 0xffffffffu;
 
@@ -440,15 +657,17 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             int bytes = 0;
             if (r < t.R) {
                 const int sq = t.seq0 + r / G, h = t.g * G + r % G;
-                src = qg + ((size_t)sq * a.num_heads + h) * D + c * 8;
+                src = qg + ((size_t)sq * a.num_heads + h) * D + c * (16 / (int)sizeof(T));
                 bytes = 16;
             }
-            cp_async16(qaddr + swz_offset<kSpRows<D>>(r, c), src, bytes);
+            cp_async16(qaddr + swz_offset<kSpRows<T, D>>(r, c), src, bytes);
         }
         cp_async_commit();
     };
 
-    SpMma<T, D, BS> path;
+    constexpr bool kF32 = sizeof(T) == 4;  // fp32 storage: TF32 tiles
+    using Path = std::conditional_t<kF32, SpTf32<D, BS>, SpMma<T, D, BS>>;
+    Path path;
     unsigned ctr = 0;  // blocks this warp has consumed (stage ring position, across items)
     int j0 = fetch();
     if (j0 < total) {
@@ -525,14 +744,18 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                     const int nvalid = min(BS, it.tok_end - (it.b0 + i) * BS);
                     const uint32_t kaddr = smem_u32(wstage + (kk % NST) * Gm::kStageBytes);
                     const uint32_t vaddr = kaddr + Gm::kTileBytes;
+                    // P between the scores and P V: two 16-row tiles of 16-bit
+                    // pairs, or the two 8-token k-steps of a TF32 tile
                     uint32_t ph[2][4], pl[2][4];
                     auto &ph1 = reinterpret_cast<uint32_t(&)[1][4]>(ph);
                     auto &pl1 = reinterpret_cast<uint32_t(&)[1][4]>(pl);
                     if (valid) {
-                        if (kSpTiles<D> == 2 && two)
-                            path.template scores<2, kSpRows<D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph, pl);
+                        if constexpr (kF32)
+                            path.template scores<kSpRows<T, D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph, pl);
+                        else if (kSpTiles<T, D> == 2 && two)
+                            path.template scores<2, kSpRows<T, D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph, pl);
                         else
-                            path.template scores<1, kSpRows<D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph1, pl1);
+                            path.template scores<1, kSpRows<T, D>>(kaddr, qaddr, 0, nvalid, a.scale_log2, lane, ph1, pl1);
                     }
                     int ng = -1, npb = -1, nrun = 0;
                     if (i + NST < it.nb) {
@@ -556,7 +779,9 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                     if (!ok) break;
                     if (valid) {
                         if (nvalid < 16) path.zero_tail(vaddr, 0, nvalid, lane);
-                        if (kSpTiles<D> == 2 && two)
+                        if constexpr (kF32)
+                            path.accumulate(vaddr, 0, lane, ph, pl);
+                        else if (kSpTiles<T, D> == 2 && two)
                             path.template accumulate<2>(vaddr, 0, lane, ph, pl);
                         else
                             path.template accumulate<1>(vaddr, 0, lane, ph1, pl1);
@@ -579,15 +804,15 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                 if (pb >= 0 && pb < a.num_blocks) {
                     const int nvalid = min(BS, it.tok_end - (it.b0 + i) * BS);
                     const uint32_t kaddr = smem_u32(wstage + (kk % NST) * Gm::kStageBytes);
-                    if constexpr (kSpTiles<D> == 2) {
+                    if constexpr (kSpTiles<T, D> == 2) {
                         if (two)
-                            path.template block<2, kSpRows<D>>(kaddr, kaddr + Gm::kTileBytes, qaddr,
+                            path.template block<2, kSpRows<T, D>>(kaddr, kaddr + Gm::kTileBytes, qaddr,
                                                                nvalid, a.scale_log2, lane);
                         else
-                            path.template block<1, kSpRows<D>>(kaddr, kaddr + Gm::kTileBytes, qaddr,
+                            path.template block<1, kSpRows<T, D>>(kaddr, kaddr + Gm::kTileBytes, qaddr,
                                                                nvalid, a.scale_log2, lane);
                     } else {
-                        path.template block<1, kSpRows<D>>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
+                        path.template block<1, kSpRows<T, D>>(kaddr, kaddr + Gm::kTileBytes, qaddr, nvalid,
                                                            a.scale_log2, lane);
                     }
                 }
@@ -644,7 +869,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             // epilogue: rows gid and gid+8 of each tile, straight from registers
             const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
-            for (int t = 0; t < kSpTiles<D>; ++t) {
+            for (int t = 0; t < kSpTiles<T, D>; ++t) {
                 if (t == 1 && !two) break;
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
@@ -656,18 +881,34 @@ __global__ void __launch_bounds__(kSpWarps * 32)
                     if (r < it.R) {
                         const float invL = L > 0.f ? 1.f / L : 0.f;
                         const size_t sh = (size_t)(it.seq0 + r / G) * a.num_heads + it.g * G + r % G;
+                        const size_t pi = sh * a.num_slots + it.slot;
+                        if (npr != 1 && tig == 0)
+                            a.ws_lse[pi] = L > 0.f ? path.m[t][hr] + __log2f(L) : -CUDART_INF_F;
+                        if constexpr (kF32) {
+                            // TF32 tiles: C elements 0 and 1 are head columns 4 apart
 #pragma unroll
-                        for (int n = 0; n < ND; ++n) {
-                            const int d = n * 8 + 2 * tig;
-                            const float2 v = make_float2(path.o[t][n][2 * hr] * invL,
-                                                         path.o[t][n][2 * hr + 1] * invL);
-                            if (npr == 1) {
-                                store_out2(a.out, sh * D + d, v.x, v.y, a.out_dtype);
-                            } else {
-                                const size_t pi = sh * a.num_slots + it.slot;
-                                *reinterpret_cast<float2 *>(a.ws_o + pi * D + d) = v;
-                                if (n == 0 && tig == 0)
-                                    a.ws_lse[pi] = L > 0.f ? path.m[t][hr] + __log2f(L) : -CUDART_INF_F;
+                            for (int g = 0; g < D / 32; ++g)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                                    for (int e = 0; e < 2; ++e) {
+                                        const int d = path.col(g, j, e);
+                                        const float v = path.o[g][j][2 * hr + e] * invL;
+                                        if (npr == 1)
+                                            store_out(a.out, sh * D + d, v, a.out_dtype);
+                                        else
+                                            a.ws_o[pi * D + d] = v;
+                                    }
+                        } else {
+#pragma unroll
+                            for (int n = 0; n < ND; ++n) {
+                                const int d = n * 8 + 2 * tig;
+                                const float2 v = make_float2(path.o[t][n][2 * hr] * invL,
+                                                             path.o[t][n][2 * hr + 1] * invL);
+                                if (npr == 1)
+                                    store_out2(a.out, sh * D + d, v.x, v.y, a.out_dtype);
+                                else
+                                    *reinterpret_cast<float2 *>(a.ws_o + pi * D + d) = v;
                             }
                         }
                     }
@@ -686,7 +927,7 @@ __global__ void __launch_bounds__(kSpWarps * 32)
 template <typename T, int D, int BS>
 pkv_status launch_sp_one(const SpLaunch &L) {
     auto kern = shared_prefix_decode_kernel<T, D, BS>;
-    constexpr int smem = SpSmem<D, BS>::kBytes;
+    constexpr int smem = SpSmem<T, D, BS>::kBytes;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     static unsigned long long done_mask = 0ull;
     static int per_sm[64];

@@ -187,7 +187,7 @@ def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib):
     assert _sp_decode(lib, pool, partition=24) == E                  # not a block multiple
     assert _sp_decode(lib, pool, num_kv_heads=4) == E                # != pool heads
     assert _sp_decode(lib, pool, scale=float("inf")) == E
-    assert _sp_decode(lib, _fake_pool(dtype=pagedkv.F32)) == U       # bf16 or fp16 pools only
+    assert _sp_decode(lib, _fake_pool(dtype=pagedkv.F32, head_dim=256)) == U  # fp32 up to 128
     # a 256-wide head passes the shape checks (here it stops at the missing workspace)
     assert _sp_decode(lib, _fake_pool(head_dim=256), ws_bytes=0) == pagedkv.ERR_WORKSPACE
     assert _sp_decode(lib, pool, num_heads=34) == U                  # group 17 > 16
@@ -248,7 +248,7 @@ def test_shared_prefix_plan_and_run_reject_bad_arguments_on_host(lib):
     assert plan(pool, gs=0x5002) == E
     assert plan(pool, pt=24) == E
     assert plan(pool, wsb=16) == pagedkv.ERR_WORKSPACE
-    assert plan(_fake_pool(dtype=pagedkv.F32)) == U
+    assert plan(_fake_pool(dtype=pagedkv.F32, head_dim=256)) == U  # fp32 up to head size 128
     assert plan(pool, S=0) == pagedkv.OK
     assert run(None) == E
     assert run(pool, out=0) == E

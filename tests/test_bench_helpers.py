@@ -79,10 +79,12 @@ def test_block_size_override_keeps_lengths_and_sizes_the_table():
 
 
 def test_shared_prefix_shapes_the_bench_routes(bench):
-    w = workload.make("tiny_f32")
-    assert not bench.shared_prefix_supported(w)  # fp32 pools take the plain decode
+    assert bench.shared_prefix_supported(workload.make("tiny_f32"))  # fp32, head size 64
     w16 = workload.make("tiny_f32", dtype="bf16", head_dim=128)
     assert bench.shared_prefix_supported(w16)
+    assert bench.shared_prefix_supported(workload.make("tiny_f32", dtype="bf16", head_dim=256))
+    assert not bench.shared_prefix_supported(workload.make("tiny_f32", head_dim=256))  # fp32, 256
+    assert not bench.shared_prefix_supported(workload.make("tiny_f32", block_size=8))
 
 
 def test_kernel_source_lists_name_existing_files(bench):

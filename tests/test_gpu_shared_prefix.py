@@ -320,6 +320,24 @@ def test_shared_prefix_f16(case):
         assert_close(dw.out, ref, "f16", f"{case} fp16 pools, out {out_dtype}")
 
 
+# ------------------------------------------------------------- fp32 pools
+
+@pytest.mark.parametrize("case", ["g4_eight_members", "g4_ragged_groups", "mha_g1", "g8_two_items",
+                                  "g16_pairs", "g3_odd", "d64_bs32", "big_group", "varied_groups"])
+def test_shared_prefix_f32(case):
+    """fp32 pools: TF32 tiles of 16 query rows, every product as three TF32
+    products, held to the fp32 tolerance of 1e-5."""
+    ctx, groups, H, Hkv, D, BS = CASES[case]
+    w = workload.build(case, dtype="f32", context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
+                       head_dim=D, block_size=BS, data_seed=5500, meta_seed=6500, groups=groups)
+    ref, _, _ = oracle_after_write(w)
+    for partition in (0, -1, 64):
+        for out_dtype in (torch.float32, torch.bfloat16):
+            dw = _run(w, partition, out_dtype)
+            assert pagedkv.get_device_error(dw.pool) == 0
+            assert_close(dw.out, ref, "f32", f"{case} fp32 pools, partition {partition}, out {out_dtype}")
+
+
 # ------------------------------------------------------------ random sweep
 
 def test_shared_prefix_random_sweep():
@@ -436,14 +454,19 @@ def _climbing_keys(w, rate):
     return w
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("case", ["g4_eight_members", "g8_two_items", "d64_bs32", "d256_g4",
                                   "big_group", "varied_groups"])
 def test_shared_prefix_climbing_scores(case, dtype):
     ctx, groups, H, Hkv, D, BS = CASES[case]
+    if dtype == "f32" and D > 128:
+        pytest.skip("fp32 pools are built up to head size 128")
     w = workload.build(case, dtype=dtype, context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
                        head_dim=D, block_size=BS, data_seed=5600, meta_seed=6600, groups=groups)
-    _climbing_keys(w, rate=20.0 / max(ctx))
+    # fp32 climbs half as steeply: at the full rate the scores reach ~120 in
+    # log2 units, where the fp32 rounding of the scores alone (measured on the
+    # CUDA-core path, which accumulates exactly in fp32) is at the 1e-5 tolerance
+    _climbing_keys(w, rate=(10.0 if dtype == "f32" else 20.0) / max(ctx))
     ref, _, _ = oracle_after_write(w)
     for partition in (0, 64):
         dw = _run(w, partition)
