@@ -321,7 +321,9 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
  * pkv_paged_attention_decode_shared_prefix_run: the decode and combine from
  * that plan, for one layer's pool, queries and output.  num_seqs, num_heads,
  * num_kv_heads, the block size, max_context_len, max_prefix_len and
- * partition_tokens must be those of the plan: a run whose geometry differs
+ * partition_tokens must be those of the plan, and the pool must hold as many
+ * query rows per work item as the plan's (the same head size and storage
+ * type, or ones with the same rows per item): a run whose geometry differs
  * from the plan in the workspace (or that finds no plan there) sets
  * PKV_FAULT_PREFIX and writes nothing.  Runs on one plan must be ordered on
  * the GPU (one stream): each run's last kernel re-arms the plan for the

@@ -15,12 +15,19 @@
 //
 // Arithmetic (standard softmax attention, online form): scores in the log2
 // domain, a running max m and sum l per query row, the accumulator rescaled
-// by 2^(m_old - m_new) whenever the max grows.  Two compute paths:
+// by 2^(m_old - m_new) when the max moves.  Three compute paths:
 //   * FMA: CUDA-core dot products; a row of D elements is spread over
-//     LPT lanes (16-byte chunks), reduced with xor shuffles.
+//     LPT lanes (16-byte chunks), reduced with xor shuffles.  A CTA takes at
+//     most four rows of a group; a larger group is split over CTAs.
 //   * MMA: bf16 or fp16 mma.sync m16n8k16 with the G query rows padded to 16:
 //     S = Q K^T per block from ldmatrix'd K, then O += P V with P split into
 //     a 16-bit high part and a 16-bit remainder so the weights keep ~16 bits.
+//   * TF32 (fp32 pools, larger groups): mma.sync m16n8k8 tiles, each product
+//     as three TF32 products (high*high + high*low + low*high); every k-step's
+//     chain starts from zero and is added to the running sum in fp32.
+// The tensor-core paths keep a lazy per-row reference instead of the exact
+// running max: it moves only when a score passes it by 8 (log2 units), so
+// most blocks skip the rescale; the weights then stay below 2^8.
 // At the end the per-warp states are merged with a log-sum-exp combine in
 // shared memory; a partitioned (split) context writes normalised partials
 // and their log2-sum-exp, which lse_combine reduces.

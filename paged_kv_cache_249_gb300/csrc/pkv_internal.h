@@ -77,8 +77,9 @@ struct DecodeLaunch {
     int device;
 };
 
-// One work item of the shared-prefix decode, written by the planning kernel.
-struct SpEntry {
+// One work item of the shared-prefix decode, written by the planning kernel
+// (as two 16-byte stores).
+struct alignas(16) SpEntry {
     int seq0;      // first sequence of the item's query rows
     int nseq;      // sequences in the item (rows = nseq * group)
     int tbl_seq;   // sequence whose block-table row names the item's blocks
@@ -91,7 +92,7 @@ static_assert(sizeof(SpEntry) == 32, "work item is two 16-byte words");
 
 // Arguments of the persistent shared-prefix decode kernel.
 struct SpArgs {
-    const void *q;              // [S][H][D] pool dtype (bf16 or fp16)
+    const void *q;              // [S][H][D] pool dtype
     void *out;                  // [S][H][D] in out_dtype (fp32, bf16 or fp16)
     float *ws_o;                // [S][H][num_slots][D] partial outputs
     float *ws_lse;              // [S][H][num_slots] their log2-sum-exp
@@ -117,6 +118,7 @@ struct SpArgs {
     int num_blocks;
     int num_slots;
     int out_dtype;              // pkv_dtype of out
+    int members_per_item;       // sequences a prefix item holds (query rows per item / group)
     float scale_log2;
 };
 
@@ -125,12 +127,15 @@ struct SpArgs {
 constexpr int kSpHdrMagic = 8;
 constexpr int32_t kSpPlanMagic = 0x50504c31;  // "PPL1"
 
-// Whether the plan in the workspace was made for this call's geometry.
+// Whether the plan in the workspace was made for this call's geometry.  The
+// members per prefix item follow the pool's head size and storage type (the
+// query rows one item's tiles hold), so a plan made for another pool is
+// refused rather than read with items larger than this kernel's tiles.
 __host__ __device__ inline bool sp_plan_matches(const SpArgs &a) {
     const int32_t *h = a.count + kSpHdrMagic;
     return h[0] == kSpPlanMagic && h[1] == a.num_seqs && h[2] == a.num_heads &&
            h[3] == a.num_kv_heads && h[4] == a.block_size && h[5] == a.num_slots &&
-           h[6] == a.suffix_base;
+           h[6] == a.suffix_base && h[7] == a.members_per_item;
 }
 
 struct SpLaunch {

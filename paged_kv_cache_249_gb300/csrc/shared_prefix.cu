@@ -19,6 +19,7 @@ namespace {
 constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic)
 constexpr int kAutoSuffixPartition = 256;   // tokens per suffix item (automatic)
 constexpr int kPlanThreads = 1024;
+static_assert(kPlanThreads <= 1024, "one class-0 range per warp: at most 32 warps");
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -86,13 +87,21 @@ struct SpPlan {
     int pbp, pbs;           // staged runs (16 tokens) per prefix / suffix item
     int pbp_shift, pbs_shift;  // log2 of pbp / pbs when a power of two, else -1
     int cls_shift_p, cls_shift_s;  // size classes: (pbp - nb) >> cls_shift_p, likewise suffix
-    int members_per_item;   // floor(32 / group)
+    int members_per_item;   // floor(query rows per item / group)
     int num_heads, num_kv_heads, slots;  // recorded in the header for the run's check
     int prefix_cap;         // entries [0, prefix_cap) hold prefix items
     int suffix_cap;         // entries [prefix_cap, prefix_cap + suffix_cap) hold suffix items
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+// One work-list entry as two 16-byte stores: the planning kernel's stores come
+// from one SM, and eight 4-byte stores to scattered entries per lane held it up
+__device__ __forceinline__ void put_entry(SpEntry *dst, int4 lo, int4 hi) {
+    int4 *d = reinterpret_cast<int4 *>(dst);
+    d[0] = lo;
+    d[1] = hi;
+}
 
 // x / d for x >= 0, with a shift when d is a power of two (sh = log2 d, else -1)
 __device__ __forceinline__ int div_by(int x, int d, int sh) { return sh >= 0 ? x >> sh : x / d; }
@@ -130,6 +139,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     __shared__ int s_ctx[kPlanSmemSeqs];
     __shared__ int s_cls[2][kPlanClasses];  // items per class, then the next free entry
     __shared__ int s_tot[2];
+    __shared__ int s_w0[2][32];  // class-0 items of each warp, then its first entry
     // the decode kernel may start setting up; it waits for this grid in
     // griddepcontrol.wait before it reads anything written here
     griddep_launch();
@@ -194,31 +204,52 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         return nq;
     };
 
-    // pass 1: items per size class
+    // pass 1: items per size class.  The full-size items (class 0, most of
+    // them) are counted per warp, and each warp lists its own in one range of
+    // class 0, so they take no shared counter (32 warps adding to one
+    // shared-memory word queue behind each other)
+    int w0p = 0, w0s = 0;  // class-0 items of this warp (prefix, suffix)
 #pragma unroll 1
     for (int gi = warp; gi < ngr; gi += nwarps) {
         const PlanGroup G = group_of(gi);
-        if (G.pblk > 0 && lane == 0) {
+        if (G.pblk > 0) {
             const int pp = div_by(G.pblk + p.pbp - 1, p.pbp, p.pbp_shift);
             const int sets = (G.end - G.start + mpi - 1) / mpi;
-            if (pp > 1) atomicAdd(&s_cls[0][0], sets * (pp - 1));
-            atomicAdd(&s_cls[0][cls_p(G.pblk - (pp - 1) * p.pbp)], sets);
+            const int cl = cls_p(G.pblk - (pp - 1) * p.pbp);
+            w0p += sets * (pp - 1) + (cl == 0 ? sets : 0);
+            if (cl != 0 && lane == 0) atomicAdd(&s_cls[0][cl], sets);
         }
         int full = 0;
         for (int s = G.start + lane; s < G.end; s += 32) {
             int ctx, nb, last;
             const int nq = suffix_of(s, G.pblk, ctx, nb, last);
             if (nq == 0) continue;
-            full += nq - 1;
-            atomicAdd(&s_cls[1][cls_s(last)], 1);
+            const int cl = cls_s(last);
+            full += nq - 1 + (cl == 0 ? 1 : 0);
+            if (cl != 0) atomicAdd(&s_cls[1][cl], 1);
         }
-        full = __reduce_add_sync(FULL, full);
-        if (full > 0 && lane == 0) atomicAdd(&s_cls[1][0], full);
+        w0s += __reduce_add_sync(FULL, full);
+    }
+    if (lane == 0) {
+        s_w0[0][warp] = w0p;
+        s_w0[1][warp] = w0s;
     }
     __syncthreads();
-    // exclusive scan of the class counts: warp r for region r
+    // warp r for region r: each warp's first class-0 entry (an exclusive scan
+    // over the warps; class 0 comes first), then the exclusive scan of the
+    // class counts
     if (tid < 64) {
         const int r = tid >> 5;
+        const int w = lane < nwarps ? s_w0[r][lane] : 0;
+        int winc = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int x = __shfl_up_sync(FULL, winc, off);
+            if (lane >= off) winc += x;
+        }
+        s_w0[r][lane] = winc - w;
+        if (lane == 31) s_cls[r][0] = winc;
+        __syncwarp();
         const int c0 = s_cls[r][2 * lane], c1 = s_cls[r][2 * lane + 1];
         int inc = c0 + c1;
 #pragma unroll
@@ -233,7 +264,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     }
     __syncthreads();
 
-    // pass 2: every item at a free entry of its class
+    // pass 2: every item at a free entry of its class (class 0: the warp's range)
+    int c0p = s_w0[0][warp], c0s = s_w0[1][warp];
 #pragma unroll 1
     for (int gi = warp; gi < ngr; gi += nwarps) {
         const PlanGroup G = group_of(gi);
@@ -242,13 +274,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
             // item k of the group: member set k / pp, part k % pp; the full
             // parts of all sets take one range, the last parts another
             const int sets = (G.end - G.start + mpi - 1) / mpi;
-            int bf = 0, br = 0;
-            if (lane == 0) {
-                if (pp > 1) bf = atomicAdd(&s_cls[0][0], sets * (pp - 1));
-                br = atomicAdd(&s_cls[0][cls_p(G.pblk - (pp - 1) * p.pbp)], sets);
+            const int cl = cls_p(G.pblk - (pp - 1) * p.pbp);
+            const int bf = c0p;
+            c0p += sets * (pp - 1);
+            int br = c0p;
+            if (cl == 0) {
+                c0p += sets;
+            } else {
+                if (lane == 0) br = atomicAdd(&s_cls[0][cl], sets);
+                br = __shfl_sync(FULL, br, 0);
             }
-            bf = __shfl_sync(FULL, bf, 0);
-            br = __shfl_sync(FULL, br, 0);
             for (int k = lane; k < sets * pp; k += 32) {
                 const int set = k / pp, q = k - set * pp;
                 const int e = q < pp - 1 ? bf + set * (pp - 1) + q : br + set;
@@ -257,14 +292,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
                     continue;
                 }
                 const int m0 = G.start + set * mpi, b0 = q * p.pbp, b1 = min(G.pblk, b0 + p.pbp);
-                p.entries[e] = SpEntry{m0, min(mpi, G.end - m0), G.start, b0, b1, q, b1 * BS, 0};
+                put_entry(p.entries + e, make_int4(m0, min(mpi, G.end - m0), G.start, b0),
+                          make_int4(b1, q, b1 * BS, 0));
             }
         }
         for (int s0 = G.start; s0 < G.end; s0 += 32) {
             const int s = s0 + lane;
             int ctx = 0, nb = 0, last = 0, nq = 0;
             if (s < G.end) nq = suffix_of(s, G.pblk, ctx, nb, last);
-            // full items: one range for the warp, split by an exclusive scan
+            // class-0 entries of these 32 members: the full items (split by an
+            // exclusive scan), then the last items that are full-size too
             const int nf = nq > 0 ? nq - 1 : 0;
             int inc = nf;
 #pragma unroll
@@ -273,10 +310,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
                 if (lane >= off) inc += x;
             }
             const int tot = __shfl_sync(FULL, inc, 31);
-            int base = 0;
-            if (lane == 0 && tot > 0) base = atomicAdd(&s_cls[1][0], tot);
-            base = __shfl_sync(FULL, base, 0) + inc - nf;
-            const int fr = nq > 0 ? atomicAdd(&s_cls[1][cls_s(last)], 1) : 0;
+            const int base = c0s + inc - nf;
+            const int cl = nq > 0 ? cls_s(last) : -1;
+            const unsigned full_last = __ballot_sync(FULL, cl == 0);
+            int fr = c0s + tot + __popc(full_last & ((1u << lane) - 1u));
+            c0s += tot + __popc(full_last);
+            if (cl > 0) fr = atomicAdd(&s_cls[1][cl], 1);
             for (int q = 0; q < nq; ++q) {
                 const int f = q < nq - 1 ? base + q : fr;
                 if (f >= p.suffix_cap) {
@@ -284,12 +323,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
                     continue;
                 }
                 const int b0 = G.pblk + q * p.pbs, b1 = min(nb, b0 + p.pbs);
-                p.entries[p.prefix_cap + f] = SpEntry{s, 1, s, b0, b1, pp + q, ctx, 0};
+                put_entry(p.entries + p.prefix_cap + f, make_int4(s, 1, s, b0), make_int4(b1, pp + q, ctx, 0));
             }
             if (s < G.end) {
                 p.nparts[s] = pp + nq;
-                p.share[2 * s] = G.start;
-                p.share[2 * s + 1] = G.pblk;
+                reinterpret_cast<int2 *>(p.share)[s] = make_int2(G.start, G.pblk);
             }
         }
     }
@@ -305,6 +343,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         p.header[kSpHdrMagic + 4] = p.block_size;
         p.header[kSpHdrMagic + 5] = p.slots;
         p.header[kSpHdrMagic + 6] = p.prefix_cap;
+        p.header[kSpHdrMagic + 7] = p.members_per_item;
     }
 }
 
@@ -532,6 +571,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     a.num_blocks = pool->num_blocks;
     a.num_slots = c.z.slots;
     a.out_dtype = out_dtype;
+    a.members_per_item = sp_rows_for(pool->head_dim, pool->dtype == PKV_F32 ? 4 : 2) / c.group;
     a.scale_log2 = scale * 1.4426950408889634f;
 
     CUtensorMap maps[2];

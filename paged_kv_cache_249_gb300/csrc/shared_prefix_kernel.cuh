@@ -9,7 +9,8 @@
 // then needs to come from HBM once for the whole group, not once per
 // sequence: a "prefix item" stages a block once and multiplies it against
 // the query rows of every member (members x GQA group <= 32 rows, two 16-row
-// mma.sync tiles; 16 rows, one tile, for 64- and 256-wide heads), while "suffix
+// mma.sync tiles; 16 rows, one tile, for 64- and 256-wide heads and for fp32
+// pools, whose tiles are TF32 with three products each), while "suffix
 // items" walk each sequence's own blocks.
 // Every item leaves a normalised partial output and its log2-sum-exp per
 // query row (or the final row when it is the sequence's only part); the
@@ -44,6 +45,7 @@ constexpr int kSpTiles = kSpRows<T, D> / 16;
 // ring takes the stages that fit: two for a 128-wide head, two for a 64-wide
 // one, and one 16 KiB stage for a 256-wide head, whose eight warps per SM then
 // hide more latency than two stages for four warps would (one CTA per SM).
+// fp32 pools (twice the bytes a stage) fit one stage for both head sizes.
 template <int D>
 constexpr int kSpSmemTarget = D == 64 ? 55 * 1024 : 112 * 1024;
 

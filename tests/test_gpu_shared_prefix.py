@@ -214,6 +214,38 @@ def test_run_without_or_against_another_plan_is_reported():
     assert pagedkv.get_device_error(dw.pool) & pagedkv.FAULT_PREFIX
 
 
+
+@pytest.mark.parametrize("plan_dtype,plan_d,run_dtype,run_d", [
+    ("bf16", 128, "bf16", 64),   # 32 query rows per item against a kernel of 16
+    ("bf16", 128, "f32", 128),   # the same head size, fp32 storage: 16 rows per item
+    ("bf16", 64, "bf16", 128),
+])
+def test_run_against_a_plan_for_another_pool_is_reported(plan_dtype, plan_d, run_dtype, run_d):
+    """A plan records the members its prefix items hold, which follow the
+    pool's head size and storage type; a run with a pool of other rows per
+    item writes nothing and reports the plan as not its own."""
+    ctx, groups, H, Hkv, D, BS = CASES["g4_eight_members"]
+    mk = lambda name, dt, d: workload.build(  # noqa: E731
+        name, dtype=dt, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=d,
+        block_size=BS, data_seed=5023, meta_seed=6023, groups=groups)
+    dp = pagedkv.DeviceWorkload(mk("plan", plan_dtype, plan_d))
+    dp.shared_prefix_setup(partition_tokens=0)
+    dr = pagedkv.DeviceWorkload(mk("run", run_dtype, run_d))
+    dr.shared_prefix_setup(partition_tokens=0)
+    ws = torch.zeros(max(dp.sp_workspace.numel(), dr.sp_workspace.numel()), dtype=torch.uint8,
+                     device=dp.sp_workspace.device)
+    dp.sp_workspace = ws
+    dr.sp_workspace = ws
+    dp.shared_prefix_plan()
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dp.pool) == 0
+    dr.out.fill_(7.0)
+    dr.decode_shared_prefix_run()
+    torch.cuda.synchronize()
+    assert pagedkv.get_device_error(dr.pool) & pagedkv.FAULT_PREFIX
+    assert float(dr.out.min()) == 7.0 == float(dr.out.max())  # nothing written
+
+
 # ------------------------------------------------------------ the work list
 
 def _expected_items(w, pbp, pbs):
