@@ -146,6 +146,7 @@ struct SpLaunch {
     int block_size;
     cudaStream_t stream;
     int device;
+    int *grid_warps;            // if set: store the persistent grid's warps here, launch nothing
 };
 
 pkv_status launch_shared_prefix_d64(const SpLaunch &L);       // bf16 pools

@@ -16,7 +16,14 @@ namespace {
 // Automatic part sizes.  Prefix items carry up to 32 query rows and are
 // the long ones; suffix items (one sequence's own blocks, G rows) are cut
 // finer so the persistent grid ends on short items.
-constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic)
+// Automatic prefix parts: the planning kernel takes the longest of 512, 1024
+// and 2048 tokens that still gives the decode grid three prefix items for
+// every four warps (fewer parts mean fewer partials to merge and fewer item
+// starts, but with fewer items than warps the grid's warps are not all busy
+// on long items and the list does not balance).  The workspace is sized for
+// the shortest.
+constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic, shortest)
+constexpr int kPlanPrefixLevels = 3;        // automatic prefix parts: 512 << 0..2 tokens
 constexpr int kAutoSuffixPartition = 256;   // tokens per suffix item (automatic)
 constexpr int kPlanThreads = 1024;
 static_assert(kPlanThreads <= 1024, "one class-0 range per warp: at most 32 warps");
@@ -27,13 +34,15 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Partition sizes in tokens (prefix, suffix) and the partial slots a sequence
 // can need: ceil(max_prefix / ptp) + ceil(max_context / pts).
 struct SpSizes {
-    int ptp, pts;      // tokens; -1 = one part
+    int ptp, pts;      // tokens; -1 = one part (ptp: the shortest prefix part when automatic)
     int pp, ps;        // most prefix / suffix parts of one sequence
     int slots;
+    bool auto_prefix;  // the planning kernel chooses the prefix part size
 };
 
 SpSizes sp_sizes(int partition_tokens, int max_context_len, int max_prefix_len) {
     SpSizes z;
+    z.auto_prefix = partition_tokens == 0;
     const int maxp = max_prefix_len < max_context_len ? max_prefix_len : max_context_len;
     int pp, ps;
     if (partition_tokens < 0) {
@@ -84,9 +93,12 @@ struct SpPlan {
     int ctx_cap;            // context lengths are clamped to [0, ctx_cap]
     int max_prefix_len;     // tokens (already capped by max_context_len)
     int block_size;         // tokens per pool block (a shared prefix is whole blocks)
-    int pbp, pbs;           // staged runs (16 tokens) per prefix / suffix item
+    int pbp, pbs;           // staged runs (16 tokens) per prefix / suffix item (pbp: the
+                            // shortest candidate; candidate k is pbp << k, k < pbp_levels)
+    int pbp_levels;         // candidate prefix part sizes (1 when the caller fixed them)
+    int target_entries;     // the longest candidate with at least this many prefix entries wins
     int pbp_shift, pbs_shift;  // log2 of pbp / pbs when a power of two, else -1
-    int cls_shift_p, cls_shift_s;  // size classes: (pbp - nb) >> cls_shift_p, likewise suffix
+    int cls_shift_s;        // suffix size classes: (pbs - nb) >> cls_shift_s
     int members_per_item;   // floor(query rows per item / group)
     int num_heads, num_kv_heads, slots;  // recorded in the header for the run's check
     int prefix_cap;         // entries [0, prefix_cap) hold prefix items
@@ -136,16 +148,24 @@ struct PlanGroup {
 // kPlanSmemSeqs sequences; a larger batch reads them where they are needed).
 __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(const SpPlan p) {
     constexpr unsigned FULL = 0xffffffffu;
+    constexpr int L = kPlanPrefixLevels;
     __shared__ int s_ctx[kPlanSmemSeqs];
-    __shared__ int s_cls[2][kPlanClasses];  // items per class, then the next free entry
+    // items per class (prefix items once for every candidate part size), then
+    // the next free entry
+    __shared__ int s_clsp[L][kPlanClasses];
+    __shared__ int s_clss[kPlanClasses];
     __shared__ int s_tot[2];
-    __shared__ int s_w0[2][32];  // class-0 items of each warp, then its first entry
+    // class-0 items of each warp, then its first entry (prefix: per candidate)
+    __shared__ int s_w0p[L][32], s_w0s[32];
+    __shared__ int s_pit[L][32];  // prefix entries of each warp's groups, per candidate
+    __shared__ int s_level;       // the candidate taken
     // the decode kernel may start setting up; it waits for this grid in
     // griddepcontrol.wait before it reads anything written here
     griddep_launch();
     griddep_wait();  // inputs written by the kernel before this one are complete
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    if (tid < 2 * kPlanClasses) (&s_cls[0][0])[tid] = 0;
+    if (tid < L * kPlanClasses) (&s_clsp[0][0])[tid] = 0;
+    else if (tid < (L + 1) * kPlanClasses) s_clss[tid - L * kPlanClasses] = 0;
     const bool staged = p.num_seqs <= kPlanSmemSeqs;
     bool bad = false;
     for (int i = tid; i <= p.num_groups || i < p.num_seqs; i += blockDim.x) {
@@ -191,7 +211,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         if (G.end - G.start >= 2) G.pblk = plen / BS;  // one member: nothing to share
         return G;
     };
-    auto cls_p = [&](int nb) { return (p.pbp - nb) >> p.cls_shift_p; };
+    // candidate prefix part k: pbp << k runs, its shift when a power of two,
+    // and the shift that maps its item sizes onto kPlanClasses classes
+    auto pb_of = [&](int k) { return p.pbp << k; };
+    auto pbsh_of = [&](int k) { return p.pbp_shift >= 0 ? p.pbp_shift + k : -1; };
+    auto clsh_of = [&](int k) {
+        int sh = 0;
+        while (((pb_of(k) - 1) >> sh) >= kPlanClasses) ++sh;
+        return sh;
+    };
     auto cls_s = [&](int nb) { return (p.pbs - nb) >> p.cls_shift_s; };
     // suffix items of sequence s (nq; the last one has `last` runs)
     auto suffix_of = [&](int s, int pblk, int &ctx, int &nb, int &last) -> int {
@@ -208,16 +236,27 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
     // them) are counted per warp, and each warp lists its own in one range of
     // class 0, so they take no shared counter (32 warps adding to one
     // shared-memory word queue behind each other)
-    int w0p = 0, w0s = 0;  // class-0 items of this warp (prefix, suffix)
+    // class-0 items and prefix entries of this warp's groups, per candidate
+    // prefix part size; class-0 suffix items
+    int w0p[L], pit[L], w0s = 0;
+#pragma unroll
+    for (int k = 0; k < L; ++k) w0p[k] = pit[k] = 0;
 #pragma unroll 1
     for (int gi = warp; gi < ngr; gi += nwarps) {
         const PlanGroup G = group_of(gi);
         if (G.pblk > 0) {
-            const int pp = div_by(G.pblk + p.pbp - 1, p.pbp, p.pbp_shift);
             const int sets = (G.end - G.start + mpi - 1) / mpi;
-            const int cl = cls_p(G.pblk - (pp - 1) * p.pbp);
-            w0p += sets * (pp - 1) + (cl == 0 ? sets : 0);
-            if (cl != 0 && lane == 0) atomicAdd(&s_cls[0][cl], sets);
+#pragma unroll
+            for (int k = 0; k < L; ++k) {
+                if (k < p.pbp_levels) {
+                    const int pb = pb_of(k);
+                    const int pp = div_by(G.pblk + pb - 1, pb, pbsh_of(k));
+                    const int cl = (pb - (G.pblk - (pp - 1) * pb)) >> clsh_of(k);
+                    w0p[k] += sets * (pp - 1) + (cl == 0 ? sets : 0);
+                    pit[k] += sets * pp;
+                    if (cl != 0 && lane == k) atomicAdd(&s_clsp[k][cl], sets);
+                }
+            }
         }
         int full = 0;
         for (int s = G.start + lane; s < G.end; s += 32) {
@@ -226,31 +265,47 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
             if (nq == 0) continue;
             const int cl = cls_s(last);
             full += nq - 1 + (cl == 0 ? 1 : 0);
-            if (cl != 0) atomicAdd(&s_cls[1][cl], 1);
+            if (cl != 0) atomicAdd(&s_clss[cl], 1);
         }
         w0s += __reduce_add_sync(FULL, full);
     }
     if (lane == 0) {
-        s_w0[0][warp] = w0p;
-        s_w0[1][warp] = w0s;
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            s_w0p[k][warp] = w0p[k];
+            s_pit[k][warp] = pit[k];
+        }
+        s_w0s[warp] = w0s;
     }
     __syncthreads();
-    // warp r for region r: each warp's first class-0 entry (an exclusive scan
-    // over the warps; class 0 comes first), then the exclusive scan of the
-    // class counts
+    // warp r for region r: the prefix part size (warp 0: the longest candidate
+    // that still gives the decode grid target_entries prefix entries; their
+    // number falls as the parts grow), each warp's first class-0 entry (an
+    // exclusive scan over the warps; class 0 comes first), then the exclusive
+    // scan of the class counts
     if (tid < 64) {
         const int r = tid >> 5;
-        const int w = lane < nwarps ? s_w0[r][lane] : 0;
+        int level = 0;
+        if (r == 0) {
+            for (int k = 1; k < p.pbp_levels; ++k) {
+                const int tot = __reduce_add_sync(FULL, lane < nwarps ? s_pit[k][lane] : 0);
+                if (tot >= p.target_entries) level = k;
+            }
+            if (lane == 0) s_level = level;
+        }
+        int *w0a = r == 0 ? s_w0p[level] : s_w0s;
+        int *cls = r == 0 ? s_clsp[level] : s_clss;
+        const int w = lane < nwarps ? w0a[lane] : 0;
         int winc = w;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int x = __shfl_up_sync(FULL, winc, off);
             if (lane >= off) winc += x;
         }
-        s_w0[r][lane] = winc - w;
-        if (lane == 31) s_cls[r][0] = winc;
+        w0a[lane] = winc - w;
+        if (lane == 31) cls[0] = winc;
         __syncwarp();
-        const int c0 = s_cls[r][2 * lane], c1 = s_cls[r][2 * lane + 1];
+        const int c0 = cls[2 * lane], c1 = cls[2 * lane + 1];
         int inc = c0 + c1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -258,30 +313,32 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
             if (lane >= off) inc += x;
         }
         const int ex = inc - c0 - c1;
-        s_cls[r][2 * lane] = ex;
-        s_cls[r][2 * lane + 1] = ex + c0;
+        cls[2 * lane] = ex;
+        cls[2 * lane + 1] = ex + c0;
         if (lane == 31) s_tot[r] = inc;
     }
     __syncthreads();
 
     // pass 2: every item at a free entry of its class (class 0: the warp's range)
-    int c0p = s_w0[0][warp], c0s = s_w0[1][warp];
+    const int level = s_level;
+    const int pbp = pb_of(level), pbp_sh = pbsh_of(level), clsh_p = clsh_of(level);
+    int c0p = s_w0p[level][warp], c0s = s_w0s[warp];
 #pragma unroll 1
     for (int gi = warp; gi < ngr; gi += nwarps) {
         const PlanGroup G = group_of(gi);
-        const int pp = div_by(G.pblk + p.pbp - 1, p.pbp, p.pbp_shift);
+        const int pp = div_by(G.pblk + pbp - 1, pbp, pbp_sh);
         if (pp > 0) {
             // item k of the group: member set k / pp, part k % pp; the full
             // parts of all sets take one range, the last parts another
             const int sets = (G.end - G.start + mpi - 1) / mpi;
-            const int cl = cls_p(G.pblk - (pp - 1) * p.pbp);
+            const int cl = (pbp - (G.pblk - (pp - 1) * pbp)) >> clsh_p;
             const int bf = c0p;
             c0p += sets * (pp - 1);
             int br = c0p;
             if (cl == 0) {
                 c0p += sets;
             } else {
-                if (lane == 0) br = atomicAdd(&s_cls[0][cl], sets);
+                if (lane == 0) br = atomicAdd(&s_clsp[level][cl], sets);
                 br = __shfl_sync(FULL, br, 0);
             }
             for (int k = lane; k < sets * pp; k += 32) {
@@ -291,7 +348,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
                     raise_fault(p.dev_error, PKV_FAULT_PREFIX);
                     continue;
                 }
-                const int m0 = G.start + set * mpi, b0 = q * p.pbp, b1 = min(G.pblk, b0 + p.pbp);
+                const int m0 = G.start + set * mpi, b0 = q * pbp, b1 = min(G.pblk, b0 + pbp);
                 put_entry(p.entries + e, make_int4(m0, min(mpi, G.end - m0), G.start, b0),
                           make_int4(b1, q, b1 * BS, 0));
             }
@@ -315,7 +372,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
             const unsigned full_last = __ballot_sync(FULL, cl == 0);
             int fr = c0s + tot + __popc(full_last & ((1u << lane) - 1u));
             c0s += tot + __popc(full_last);
-            if (cl > 0) fr = atomicAdd(&s_cls[1][cl], 1);
+            if (cl > 0) fr = atomicAdd(&s_clss[cl], 1);
             for (int q = 0; q < nq; ++q) {
                 const int f = q < nq - 1 ? base + q : fr;
                 if (f >= p.suffix_cap) {
@@ -495,6 +552,18 @@ pkv_status sp_prepare(const pkv_pool *pool, int num_seqs, int num_heads, int num
     return PKV_OK;
 }
 
+// The decode kernel instance for the pool's storage type and head size.
+pkv_status sp_dispatch(const pkv_pool *pool, const SpLaunch &L) {
+    const int hd = pool->head_dim;
+    if (pool->dtype == PKV_F32)
+        return hd == 64 ? launch_shared_prefix_f32_d64(L) : launch_shared_prefix_f32_d128(L);
+    if (pool->dtype == PKV_F16)
+        return hd == 64 ? launch_shared_prefix_f16_d64(L)
+                        : (hd == 128 ? launch_shared_prefix_f16_d128(L) : launch_shared_prefix_f16_d256(L));
+    return hd == 64 ? launch_shared_prefix_d64(L)
+                    : (hd == 128 ? launch_shared_prefix_d128(L) : launch_shared_prefix_d256(L));
+}
+
 pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_heads,
                    const int32_t *context_lens, const int32_t *group_starts,
                    const int32_t *prefix_lens, int num_groups, void *workspace, cudaStream_t st) {
@@ -527,7 +596,6 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
         while (((cap - 1) >> sh) >= kPlanClasses) ++sh;
         return sh;
     };
-    p.cls_shift_p = cls_shift(p.pbp);
     p.cls_shift_s = cls_shift(p.pbs);
     auto pow2_shift = [](int d) {
         int sh = 0;
@@ -535,6 +603,23 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
         return (1 << sh) == d ? sh : -1;
     };
     p.pbp_shift = pow2_shift(p.pbp);
+    // automatic prefix parts: the kernel tries pbp << 0..kPlanPrefixLevels-1
+    // and keeps three prefix items for every four warps of the decode grid
+    p.pbp_levels = 1;
+    p.target_entries = 0;
+    if (c.z.auto_prefix) {
+        int warps = 0;
+        SpLaunch q;
+        std::memset(&q, 0, sizeof(q));
+        q.head_dim = pool->head_dim;
+        q.block_size = c.U;
+        q.device = c.dev;
+        q.grid_warps = &warps;
+        const pkv_status qs = sp_dispatch(pool, q);
+        if (qs != PKV_OK) return qs;
+        p.pbp_levels = kPlanPrefixLevels;
+        p.target_entries = (3 * warps + 4 * pool->num_kv_heads - 1) / (4 * pool->num_kv_heads);
+    }
     p.pbs_shift = pow2_shift(p.pbs);
     p.prefix_cap = num_seqs * c.z.pp;
     p.suffix_cap = num_seqs * c.z.ps;
@@ -577,6 +662,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     CUtensorMap maps[2];
     std::memcpy(maps, pool->tma, sizeof(maps));
     SpLaunch L;
+    std::memset(&L, 0, sizeof(L));
     L.tmk = &maps[0];
     L.tmv = &maps[1];
     L.args = a;
@@ -585,14 +671,7 @@ pkv_status sp_run(const pkv_pool *pool, const SpCall &c, void *out, pkv_dtype ou
     L.stream = st;
     L.device = c.dev;
     const int hd = pool->head_dim;
-    const pkv_status s1 =
-        pool->dtype == PKV_F32
-            ? (hd == 64 ? launch_shared_prefix_f32_d64(L) : launch_shared_prefix_f32_d128(L))
-        : pool->dtype == PKV_F16
-            ? (hd == 64 ? launch_shared_prefix_f16_d64(L)
-                        : (hd == 128 ? launch_shared_prefix_f16_d128(L) : launch_shared_prefix_f16_d256(L)))
-            : (hd == 64 ? launch_shared_prefix_d64(L)
-                        : (hd == 128 ? launch_shared_prefix_d128(L) : launch_shared_prefix_d256(L)));
+    const pkv_status s1 = sp_dispatch(pool, L);
     if (s1 != PKV_OK) return s1;
 
     // the combine waits for the decode grid in griddepcontrol.wait, then

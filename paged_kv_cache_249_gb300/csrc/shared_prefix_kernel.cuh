@@ -946,6 +946,10 @@ pkv_status launch_sp_one(const SpLaunch &L) {
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
     }
     const int grid = __atomic_load_n(&per_sm[L.device & 63], __ATOMIC_RELAXED) * sm_count(L.device);
+    if (L.grid_warps) {
+        *L.grid_warps = grid * kSpWarps;
+        return PKV_OK;
+    }
     // launched as a programmatic dependent of the planning kernel: the CTAs
     // set up while the plan finishes and wait for it in griddepcontrol.wait
     return cuda_status(

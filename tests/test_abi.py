@@ -196,8 +196,9 @@ def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib):
 
 def test_shared_prefix_workspace_bytes(lib):
     """Header, per-sequence counts and sharing records, the work list, and
-    the partials: one slot per prefix part (512-token parts by default) and
-    per own part (256 tokens by default) of the longest sequence."""
+    the partials: one slot per prefix part (sized for 512-token parts, the
+    shortest the automatic choice takes) and per own part (256 tokens by
+    default) of the longest sequence."""
     r = lambda x: -(-x // 256) * 256  # noqa: E731
 
     def expect(S, H, D, maxc, maxp, pt):
