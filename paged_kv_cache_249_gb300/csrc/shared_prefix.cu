@@ -18,10 +18,11 @@ namespace {
 // finer so the persistent grid ends on short items.
 // Automatic prefix parts: the planning kernel takes the longest of 512, 1024
 // and 2048 tokens that still gives the decode grid three prefix items for
-// every four warps (fewer parts mean fewer partials to merge and fewer item
-// starts, but with fewer items than warps the grid's warps are not all busy
-// on long items and the list does not balance).  The workspace is sized for
-// the shortest.
+// every four warps, or for every two warps with fp32 pools (fewer parts mean
+// fewer partials to merge and fewer item starts, but with fewer items than
+// warps the grid's warps are not all busy on long items and the list does
+// not balance; the fp32 items, bound by their TF32 arithmetic, gain less
+// from fewer starts).  The workspace is sized for the shortest.
 constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic, shortest)
 constexpr int kPlanPrefixLevels = 3;        // automatic prefix parts: 512 << 0..2 tokens
 constexpr int kAutoSuffixPartition = 256;   // tokens per suffix item (automatic)
@@ -605,6 +606,7 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
     p.pbp_shift = pow2_shift(p.pbp);
     // automatic prefix parts: the kernel tries pbp << 0..kPlanPrefixLevels-1
     // and keeps three prefix items for every four warps of the decode grid
+    // (every two warps for fp32 pools)
     p.pbp_levels = 1;
     p.target_entries = 0;
     if (c.z.auto_prefix) {
@@ -618,7 +620,8 @@ pkv_status sp_plan(const pkv_pool *pool, const SpCall &c, int num_seqs, int num_
         const pkv_status qs = sp_dispatch(pool, q);
         if (qs != PKV_OK) return qs;
         p.pbp_levels = kPlanPrefixLevels;
-        p.target_entries = (3 * warps + 4 * pool->num_kv_heads - 1) / (4 * pool->num_kv_heads);
+        const int per = pool->dtype == PKV_F32 ? 2 : 4;  // warps per three items
+        p.target_entries = (3 * warps + per * pool->num_kv_heads - 1) / (per * pool->num_kv_heads);
     }
     p.pbs_shift = pow2_shift(p.pbs);
     p.prefix_cap = num_seqs * c.z.pp;

@@ -686,16 +686,14 @@ __global__ void __launch_bounds__(kSpWarps * 32)
             cp_async_wait_all();
             __syncwarp();  // the item's query rows are in place
             // The next item is claimed as late as its latency allows, so the
-            // longest-first list keeps balancing the warps until its end: for
-            // 128- and 256-wide heads a long item claims it three blocks before
-            // its first stage is due, reads the index a block later and
-            // decodes the entry a block after that; a short item, and every
-            // item of a 64-wide head (measured faster so, with its shorter
-            // blocks), claims it now and reads it after its first blocks.
-            // Its first stages go into the ring slots this item frees in its
-            // last NST blocks (ring positions continue across items), or
-            // after the loop if its block ids came too late.
-            const bool late = D >= 128 && it.nb > NST + 3;
+            // longest-first list keeps balancing the warps until its end: a
+            // long item claims it three blocks before its first stage is due,
+            // reads the index a block later and decodes the entry a block
+            // after that; a short item claims it now and reads it after its
+            // first blocks.  Its first stages go into the ring slots this
+            // item frees in its last NST blocks (ring positions continue
+            // across items), or after the loop if its block ids came too late.
+            const bool late = it.nb > NST + 3;
             const int claim_at = late ? it.nb - NST - 3 : -1;
             const int read_at = late ? claim_at + 1 : 0;
             int jn_raw = 0;
