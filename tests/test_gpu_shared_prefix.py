@@ -402,6 +402,41 @@ def test_shared_prefix_random_sweep():
         assert_close(dw.out, ref, dtype, f"trial {trial}: BS{BS} D{D} G{G} groups {groups} pt {pt}")
 
 
+
+@pytest.mark.parametrize("D,dtype,G", [(128, "bf16", 4), (256, "bf16", 4), (64, "f16", 8),
+                                       (128, "f32", 4)])
+def test_shared_prefix_automatic_parts_on_irregular_batches(D, dtype, G):
+    """Batches large enough that the plan takes its longer automatic prefix
+    parts (1024 or 2048 tokens), with irregular groups: one to sixteen
+    members, prefixes of any whole number of blocks (so a prefix's last part
+    is ragged) and own lengths from nothing to 700 tokens.  Every sequence
+    is checked against the oracle, and the plan's prefix items are longer
+    than the shortest candidate (512 tokens)."""
+    rng = np.random.default_rng(77 + D + (1 if dtype == "f32" else 0))
+    BS, Hkv = 16, 8
+    groups, ctx = [], []
+    while len(ctx) < 320:
+        members = int(rng.integers(1, 17))
+        prefix = BS * int(rng.integers(64, 400)) if members > 1 else 0
+        groups.append((members, prefix))
+        # at most one member ends on the prefix (two would write one shared slot)
+        own = [int(rng.integers(1, 700)) for _ in range(members)]
+        own[0] = int(rng.integers(0, 700))
+        ctx += [prefix + o for o in own]
+    w = workload.build(f"autoparts{D}{dtype}", dtype=dtype, context_lens=ctx, num_heads=Hkv * G,
+                       num_kv_heads=Hkv, head_dim=D, block_size=BS, data_seed=9300 + D,
+                       meta_seed=9400 + D, groups=groups)
+    ref, _, _ = oracle_after_write(w)
+    dw = _run(w, 0, out_dtype=torch.bfloat16)
+    assert pagedkv.get_device_error(dw.pool) == 0
+    assert_close(dw.out, ref, dtype, f"D{D} {dtype} G{G}: {len(groups)} groups, automatic parts")
+    ws = dw.sp_workspace.cpu().numpy().view(np.int32)
+    S = w.num_seqs
+    r = lambda x: -(-x // 256) * 256  # noqa: E731
+    ent = ws[(256 + r(S * 4) + r(S * 8)) // 4:].reshape(-1, 8)[:int(ws[0])]
+    assert int((ent[:, 4] - ent[:, 3]).max()) > 32, "the plan kept the shortest prefix parts"
+
+
 def test_shared_prefix_random_sweep_d256():
     """The same sweep for 256-wide heads (items of 16 rows: 16 / G members)."""
     rng = np.random.default_rng(2256)
