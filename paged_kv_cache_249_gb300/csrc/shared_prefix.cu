@@ -15,14 +15,14 @@ namespace {
 
 // Automatic part sizes.  Prefix items carry up to 32 query rows and are
 // the long ones; suffix items (one sequence's own blocks, G rows) are cut
-// finer so the persistent grid ends on short items.
-// Automatic prefix parts: the planning kernel takes the longest of 512, 1024
-// and 2048 tokens that still gives the decode grid three prefix items for
-// every four warps, or for every two warps with fp32 pools (fewer parts mean
-// fewer partials to merge and fewer item starts, but with fewer items than
-// warps the grid's warps are not all busy on long items and the list does
-// not balance; the fp32 items, bound by their TF32 arithmetic, gain less
-// from fewer starts).  The workspace is sized for the shortest.
+// finer so the persistent grid ends on short items.  For the prefix the
+// planning kernel takes the longest of 512, 1024 and 2048 tokens that still
+// gives the decode grid three prefix items for every four warps, or for
+// every two warps with fp32 pools (fewer parts mean fewer partials to merge
+// and fewer item starts, but with fewer items than warps the grid's warps
+// are not all busy on long items and the list does not balance; the fp32
+// items, bound by their TF32 arithmetic, gain less from fewer starts).  The
+// workspace is sized for the shortest.
 constexpr int kAutoPrefixPartition = 512;   // tokens per prefix item (automatic, shortest)
 constexpr int kPlanPrefixLevels = 3;        // automatic prefix parts: 512 << 0..2 tokens
 constexpr int kAutoSuffixPartition = 256;   // tokens per suffix item (automatic)
@@ -233,12 +233,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) shared_prefix_plan_kernel(con
         return nq;
     };
 
-    // pass 1: items per size class.  The full-size items (class 0, most of
-    // them) are counted per warp, and each warp lists its own in one range of
-    // class 0, so they take no shared counter (32 warps adding to one
-    // shared-memory word queue behind each other)
-    // class-0 items and prefix entries of this warp's groups, per candidate
-    // prefix part size; class-0 suffix items
+    // pass 1: items per size class, the prefix items once for every candidate
+    // part size.  The full-size items (class 0, most of them) are counted per
+    // warp, and each warp lists its own in one range of class 0, so they take
+    // no shared counter (32 warps adding to one shared-memory word queue
+    // behind each other).  w0p, pit: class-0 items and entries of this warp's
+    // groups per candidate; w0s: its class-0 suffix items.
     int w0p[L], pit[L], w0s = 0;
 #pragma unroll
     for (int k = 0; k < L; ++k) w0p[k] = pit[k] = 0;
