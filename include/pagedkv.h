@@ -290,9 +290,10 @@ pkv_status pkv_contiguous_attention_decode(const pkv_pool *cache, void *out, pkv
  *
  * partition_tokens: 0 = automatic (prefix parts of 512, 1024 or 2048 tokens,
  * chosen on the device: the longest that still gives the persistent decode
- * grid three prefix items for every four warps; parts of 256 tokens for each
- * sequence's own blocks), -1 = one part each, > 0 = parts of that many tokens
- * (a multiple of block_size, at most 8192).  workspace: device buffer (256-byte
+ * grid three prefix items for every four warps, every two warps for F32
+ * pools; parts of 256 tokens for each sequence's own blocks), -1 = one part
+ * each, > 0 = parts of that many tokens (a multiple of block_size, at most
+ * 8192).  workspace: device buffer (256-byte
  * aligned) of at least pkv_shared_prefix_workspace_bytes(...) bytes; it also
  * holds the work list, so every call needs one.  Supported: BF16 or F16
  * pools (head_dim 64, 128 or 256; the work items of 64- and 256-wide heads
